@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Benchmark of the W8A8 quantized linear layer on one GB300 (or N replicas).
+
+Workload: W8A8 per-channel linear, N=10240, K=2560, M in {1, 128, 1024, 4096,
+8192} (seed 0; x ~ N(0,1) fp16 with 26 of the 2560 K-channels x30, weights
+~ N(0, 0.02) quantized per output channel on the GPU before timing).  One
+step = the whole path for every M of the sweep: per-token activation
+quantization, then the INT8 GEMM (M > 1) or the INT8 matrix-vector kernel
+(M = 1) with the fused dequant to fp16.
+
+value    = sum over the sweep of 2*M*N*K integer ops / device time of the step
+           (TOPS), inputs resident in HBM; L2 is flushed (a 2 x L2 write)
+           before every call, outside the timed events.
+e2e      = the same metric through the C ABI's ``linear`` call with pinned
+           host buffers: host->device copy of x, the layer, device->host copy
+           of y, all inside the timed events.
+roofline = the dominant kernel (the GEMM at M=8192): 2*M*N*K / its average
+           CUDA-event duration over the timed steps, against the measured
+           dense fp16/bf16 tensor peak.
+cpu_baseline / --impl reference = the CPU oracle, as it stands, on a bounded
+           sample of rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from w4a8_int8_quantized_gb300 import synth  # noqa: E402
+
+WORKLOAD = synth.WORKLOADS["pc_sweep"]
+N_OUT, K_IN, MS = WORKLOAD["N"], WORKLOAD["K"], WORKLOAD["Ms"]
+METRIC = "W8A8 GEMM INT8 TOPS & ms (N=10240,K=2560,M=1..8192); decode GEMV HBM GB/s"
+UNIT = "TOPS"
+# Pages' M5 Pro per-channel latencies for this sweep (ms, "cider 소개",
+# section "cider의 성능 측정 결과"): the same metric as a whole-sweep rate.
+PAGES_MS = {1: 0.27, 128: 0.34, 1024: 1.23, 4096: 4.41, 8192: 8.71}
+PAGES_TOPS = sum(2.0 * m * N_OUT * K_IN for m in MS) / (sum(PAGES_MS.values()) * 1e-3) / 1e12
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def config_dict():
+    return {"workload": "W8A8 per-channel linear, N=10240, K=2560, M in {1,128,1024,4096,8192}",
+            "N": N_OUT, "K": K_IN, "Ms": MS, "group_size": 0,
+            "inputs": "seeded synthetic: x ~ N(0,1) fp16, 26 of 2560 K-channels x30; "
+                      "W ~ N(0,0.02) fp16 quantized to INT8 per output channel",
+            "l2": "flushed by a 2 x L2 write before every call, outside the timed events"}
+
+
+def step_ops():
+    return sum(2.0 * m * N_OUT * K_IN for m in MS)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak(d, *names):
+    """First numeric value among keys that contain one of `names`."""
+    def walk(o, prefix=""):
+        if isinstance(o, dict):
+            for k, v in o.items():
+                yield from walk(v, f"{prefix}{k}.")
+        else:
+            yield prefix[:-1], o
+    for name in names:
+        for k, v in walk(d):
+            if k.split(".")[-1] == name and isinstance(v, (int, float)):
+                return float(v)
+    return None
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------- distributed setup --
+
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws, device=None):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- CPU oracle --
+
+def oracle_sample_step(rows: int, inputs):
+    """The oracle on the first `rows` rows of every M of the sweep; returns
+    (ops, seconds)."""
+    import oracle
+    ops, t = 0.0, 0.0
+    wq, sw = inputs["wq_ref"], inputs["sw_ref"]
+    for m in MS:
+        r = min(m, rows)
+        x = inputs["x"][m][:r]
+        t0 = time.perf_counter()
+        oracle.linear(x, wq, sw)
+        t += time.perf_counter() - t0
+        ops += 2.0 * r * N_OUT * K_IN
+    return ops, t
+
+
+def host_inputs():
+    xs = {m: synth.activations(m, K_IN, seed=0, **WORKLOAD["act"]) for m in MS}
+    W = synth.weights(N_OUT, K_IN, seed=0)
+    return {"x": xs, "W": W}
+
+
+def calibrate_rows(inputs, target_s):
+    rows = 2
+    _, t = oracle_sample_step(rows, inputs)
+    want = int(rows * target_s / max(t, 1e-3))
+    return max(2, min(want, 8192)), t
+
+
+def cpu_baseline(inputs, target_s=12.0):
+    import oracle
+    oracle.build()
+    wq, sw = oracle.quantize_weight_int8(inputs["W"])
+    inputs["wq_ref"], inputs["sw_ref"] = wq, sw
+    rows, _ = calibrate_rows(inputs, target_s)
+    ops, t = oracle_sample_step(rows, inputs)
+    return {"value": ops / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {rows} rows of each M of the sweep (N=10240, K=2560) through "
+                      f"the oracle's quantize + int64 GEMM + dequant; {t:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup("gloo")
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inputs = host_inputs()
+    wq, sw = oracle.quantize_weight_int8(inputs["W"])
+    inputs["wq_ref"], inputs["sw_ref"] = wq, sw
+    # each step is a bounded sample sized so the whole run takes ~2-3 minutes
+    per_step = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    rows, _ = calibrate_rows(inputs, per_step)
+    for _ in range(args.warmup):
+        oracle_sample_step(rows, inputs)
+    ops = t = 0.0
+    for _ in range(args.steps):
+        o, s = oracle_sample_step(rows, inputs)
+        ops += o
+        t += s
+    value = ops / t / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / PAGES_TOPS, "dtype": "int8", "data": "synthetic",
+            "config": config_dict(), "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": f"first {rows} rows of each M of the sweep per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- GPU path --
+
+def run_ours(args):
+    import ctypes
+
+    import torch
+
+    ws, rank, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import w4a8_int8_quantized_gb300 as w8
+    lib = w8.load()
+    if not w8.w8a8_is_available():
+        raise RuntimeError("libw8a8 needs a compute-capability 10.3 GPU")
+
+    inputs = host_inputs()
+    stream = torch.cuda.current_stream()
+    s_ptr = ctypes.c_void_p(stream.cuda_stream)
+    P = ctypes.c_void_p
+
+    W = torch.from_numpy(inputs["W"]).to(device)
+    wq, sw = w8.quantize_weight_int8(W)
+    del W
+    bufs = {}
+    for m in MS:
+        x = torch.from_numpy(inputs["x"][m]).to(device)
+        xq = torch.empty((m, K_IN), dtype=torch.int8, device=device)
+        sa = torch.empty((m, 1), dtype=torch.float32, device=device)
+        y = torch.empty((m, N_OUT), dtype=torch.float16, device=device)
+        ws_bytes = w8.w8a8_linear_workspace_bytes(m, K_IN, 0)
+        wsb = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+        xh = torch.from_numpy(inputs["x"][m]).pin_memory()
+        yh = torch.empty((m, N_OUT), dtype=torch.float16).pin_memory()
+        bufs[m] = dict(x=x, xq=xq, sa=sa, y=y, ws=wsb, xh=xh, yh=yh)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=device)
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: status {st}")
+
+    def call_quant(m):
+        b = bufs[m]
+        check(lib.quantize_act_per_token(P(b["x"].data_ptr()), m, K_IN, 0, P(b["xq"].data_ptr()),
+                                         P(b["sa"].data_ptr()), s_ptr), "quantize")
+
+    def call_gemm(m):
+        b = bufs[m]
+        f = lib.w8a8_mv if m == 1 else lib.w8a8_gemm
+        check(f(P(b["xq"].data_ptr()), P(b["sa"].data_ptr()), P(wq.data_ptr()),
+                P(sw.data_ptr()), m, N_OUT, K_IN, 0, P(b["y"].data_ptr()), s_ptr), "gemm")
+
+    def call_linear(m, x, y):
+        b = bufs[m]
+        check(lib.linear(P(x.data_ptr()), P(wq.data_ptr()), P(sw.data_ptr()), m, N_OUT, K_IN, 0,
+                         8, P(b["ws"].data_ptr()), b["ws"].numel(), P(y.data_ptr()), s_ptr),
+              "linear")
+
+    def kernel_step(record):
+        evs = []
+        for m in MS:
+            flush.fill_(1)
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            call_quant(m)
+            e1.record(stream)
+            call_gemm(m)
+            e2.record(stream)
+            evs.append((m, e0, e1, e2))
+        if record is not None:
+            record.append(evs)
+
+    def e2e_step(record):
+        evs = []
+        for m in MS:
+            b = bufs[m]
+            flush.fill_(1)
+            e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            e0.record(stream)
+            b["x"].copy_(b["xh"], non_blocking=True)
+            call_linear(m, b["x"], b["y"])
+            b["yh"].copy_(b["y"], non_blocking=True)
+            e1.record(stream)
+            evs.append((m, e0, e1))
+        if record is not None:
+            record.append(evs)
+
+    # warm-up (also sets the kernels' shared-memory attributes)
+    for _ in range(max(3, args.warmup)):
+        kernel_step(None)
+    torch.cuda.synchronize()
+
+    peaks, peak_src = load_peaks()
+    rec = []
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        torch.cuda._sleep(int(2e6))  # queue depth: the CPU enqueues ahead of the GPU
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            kernel_step(rec)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(ws)
+    torch.cuda.synchronize()
+
+    per_m = {m: {"quant_ms": 0.0, "gemm_ms": 0.0} for m in MS}
+    for evs in rec:
+        for m, e0, e1, e2 in evs:
+            per_m[m]["quant_ms"] += e0.elapsed_time(e1)
+            per_m[m]["gemm_ms"] += e1.elapsed_time(e2)
+    step_ms = sum(v["quant_ms"] + v["gemm_ms"] for v in per_m.values()) / args.steps
+    step_ms = max_over_ranks(step_ms, ws, device)
+    value = ws * step_ops() / (step_ms * 1e-3) / 1e12
+
+    # e2e through linear() with host buffers
+    for _ in range(2):
+        e2e_step(None)
+    rec2 = []
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(2e6))
+    for _ in range(args.steps):
+        e2e_step(rec2)
+    torch.cuda.synchronize()
+    e2e_ms = sum(e0.elapsed_time(e1) for evs in rec2 for _, e0, e1 in evs) / args.steps
+    e2e_ms = max_over_ranks(e2e_ms, ws, device)
+    e2e_value = ws * step_ops() / (e2e_ms * 1e-3) / 1e12
+
+    detail = {}
+    for m in MS:
+        q = per_m[m]["quant_ms"] / args.steps
+        g = per_m[m]["gemm_ms"] / args.steps
+        d = {"quant_ms": round(q, 5), "gemm_ms": round(g, 5), "ms": round(q + g, 5),
+             "TOPS": round(2.0 * m * N_OUT * K_IN / ((q + g) * 1e-3) / 1e12, 3),
+             "gemm_TOPS": round(2.0 * m * N_OUT * K_IN / (g * 1e-3) / 1e12, 3),
+             "quant_GBps": round(m * K_IN * 3 + m * 4, 1) / (q * 1e-3) / 1e9}
+        if m == 1:
+            d["gemv_GBps"] = round((N_OUT * K_IN + N_OUT * 4 + K_IN + 4 + N_OUT * 2)
+                                   / (g * 1e-3) / 1e9, 1)
+        d["quant_GBps"] = round(d["quant_GBps"], 1)
+        detail[str(m)] = d
+
+    mdom = max(m for m in MS)
+    dom_ms = per_m[mdom]["gemm_ms"] / args.steps
+    achieved = 2.0 * mdom * N_OUT * K_IN / (dom_ms * 1e-3) / 1e12
+    peak = _peak(peaks, "bf16_tflops") if peak_src == "measured" else FALLBACK_PEAKS["bf16_tflops"]
+    if peak is None:
+        peak, peak_src = FALLBACK_PEAKS["bf16_tflops"], "fallback"
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "kernel": f"w8a8 GEMM, M={mdom}, N={N_OUT}, K={K_IN}",
+                "peak_source": f"{peak_src} dense bf16/fp16 tensor peak (burst)"}
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": round(value / PAGES_TOPS, 3), "dtype": "int8",
+            "data": "synthetic", "config": config_dict(), "roofline": roofline,
+            "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
+                    "h2d_bytes_per_step": sum(m * K_IN * 2 for m in MS),
+                    "d2h_bytes_per_step": sum(m * N_OUT * 2 for m in MS)},
+            "gpu_launches": args.steps * 2 * len(MS),
+            "clocks": clocks.summary(), "detail": detail,
+            "wall_s_timed_region": round(wall, 4)}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inputs)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the timed CPU-oracle sample (about 15 s)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,79 @@
+// Internal helpers shared by the libw8a8 translation units (not part of the
+// C ABI).  Every kernel launch goes through these checks so that argument
+// errors never reach the device.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/w8a8.h"
+
+namespace w8a8 {
+
+constexpr int kNumSMsGB300 = 152;
+
+constexpr int kMaxK = 32768;
+
+// Reads and clears the device-side error word that kernels with bounded
+// waits set when a wait gives up (the value says which wait).
+int read_and_clear_device_error(unsigned int *code);
+
+// Device address of that word on the current device (looked up once per
+// device), passed to the kernels as an argument; nullptr on failure.
+unsigned int *device_error_word();
+
+enum DeviceErrorCode : unsigned int {
+  kDevErrNone = 0,
+  kDevErrFullBarrier = 1,    // producer/MMA wait on a filled stage
+  kDevErrEmptyBarrier = 2,   // producer wait on a freed stage
+  kDevErrAccumBarrier = 3,   // epilogue wait on a finished accumulator
+  kDevErrTmemEmpty = 4,      // MMA wait on a drained accumulator
+};
+
+inline bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline int ceil_div(long a, long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Compute capability check for the current device, cached per device.
+int check_device();
+
+// Launch-error check after a kernel launch.
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA;
+}
+
+inline int groups_of(int K, int group_size) {
+  return group_size == 0 ? 1 : K / group_size;
+}
+
+inline bool valid_group_size(int K, int group_size) {
+  if (group_size == 0) return true;
+  if (group_size != 64 && group_size != 128) return false;
+  return K % group_size == 0;
+}
+
+// ---- kernel launchers (one per translation unit) ---------------------------
+
+// Row quantization: rows of fp16 -> int8 (qmax 127) or packed int4 (qmax 7,
+// packed != nullptr), one fp32 scale per row or per group.
+int launch_row_quant(const __half *x, int R, int K, int group_size, int qmax,
+                     int8_t *q, uint8_t *packed, float *scale, cudaStream_t s);
+
+// Matrix-vector products for M == 1.
+int launch_gemv_w8a8(const int8_t *xq, const float *sa, const int8_t *Wq,
+                     const float *sw, int N, int K, int group_size, __half *y,
+                     cudaStream_t s);
+int launch_gemv_w4a8(const int8_t *xq, const float *sa, const uint8_t *Wp,
+                     const float *sw, int N, int K, __half *y, cudaStream_t s);
+
+// GEMMs for M > 1.  acc_out != nullptr exports the exact int32 (per-group)
+// sums [M, N, G] instead of the fp16 output.
+int launch_gemm_mma(const int8_t *xq, const float *sa, const void *W,
+                    const float *sw, int M, int N, int K, int group_size,
+                    int wbits, __half *y, int32_t *acc_out, cudaStream_t s);
+
+}  // namespace w8a8

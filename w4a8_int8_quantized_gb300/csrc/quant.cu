@@ -1,0 +1,170 @@
+// Row quantization kernels: online per-token activation quantization and the
+// offline INT8 / INT4 weight quantizers share one kernel.
+//
+// Method: "Apple Silicon의 AI 한계치는 당신의 생각보다 높습니다", section
+// "INT8 TensorOps 커널 설계", steps 1-2 (a fast min/max reduction gives each
+// row -- or each group of 64 / 128 elements, section "입도(Granularity)" --
+// its scale; one streaming pass maps fp16 to INT8); "cider 소개", section
+// "cider의 양자화 모드와 적용 가능한 영역" (symmetric INT8 per token; INT4
+// weights packed two per uint8 for W4A8).
+//
+// Design (HBM-bound, one streaming pass): a team of T threads (one warp for
+// K <= 4096, up to 256 threads for K <= 32768) owns one row.  Each thread loads its V 16-byte vectors (8 fp16
+// each) once into registers, the team reduces absmax with warp shuffles (and
+// shared memory when T > 32), and the same registers are quantized and stored
+// as 8-byte INT8 vectors (or one 32-bit word of 8 nibbles).  Vector i of
+// thread t covers elements [8 (i T + t), 8 (i T + t) + 8): consecutive lanes
+// read consecutive 16-byte chunks, so every warp load is one fully coalesced
+// 512-byte transaction, and a group of 64 / 128 elements is 8 / 16
+// consecutive lanes of one warp, reduced with xor shuffles inside the warp.
+#include "common.cuh"
+
+namespace w8a8 {
+namespace {
+
+__device__ __forceinline__ float absmax8(const uint4 &v) {
+  const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float2 f = __half22float2(h[j]);
+    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  return m;
+}
+
+// q = clamp(rint(x / s), -qmax, qmax); IEEE division, ties to even.
+__device__ __forceinline__ int quant1(float x, float s, float amax, int qmax) {
+  if (amax == 0.f) return 0;
+  int q = __float2int_rn(__fdiv_rn(x, s));
+  return max(-qmax, min(qmax, q));
+}
+
+template <int V>
+__global__ void __launch_bounds__(256) row_quant_kernel(
+    const uint4 *__restrict__ x, long R, int K, int gs, int qmax, int T,
+    int8_t *__restrict__ q, uint32_t *__restrict__ packed,
+    float *__restrict__ scale) {
+  __shared__ float red[32];
+  const int nvec = K >> 3;
+  const int t = threadIdx.x % T;
+  const int team = threadIdx.x / T;
+  const long r = static_cast<long>(blockIdx.x) * (blockDim.x / T) + team;
+  const bool active = r < R;
+  const int G = gs == 0 ? 1 : K / gs;
+
+  uint4 v[V];
+  float vmax[V];
+  const uint4 *xr = x + r * nvec;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int vi = i * T + t;
+    if (active && vi < nvec) {
+      v[i] = __ldcs(xr + vi);
+    } else {
+      v[i] = make_uint4(0, 0, 0, 0);
+    }
+    vmax[i] = absmax8(v[i]);
+  }
+
+  float amax_row = 0.f;
+  if (gs == 0) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) amax_row = fmaxf(amax_row, vmax[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      amax_row = fmaxf(amax_row, __shfl_xor_sync(0xffffffffu, amax_row, o));
+    if (T > 32) {
+      const int warp = threadIdx.x >> 5;
+      if ((threadIdx.x & 31) == 0) red[warp] = amax_row;
+      __syncthreads();
+      const int w0 = team * (T >> 5);
+      amax_row = 0.f;
+      for (int w = 0; w < (T >> 5); ++w) amax_row = fmaxf(amax_row, red[w0 + w]);
+    }
+  } else {
+    // a group is gs/8 consecutive lanes of one warp
+    const int width = gs >> 3;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      for (int o = width >> 1; o > 0; o >>= 1)
+        vmax[i] = fmaxf(vmax[i], __shfl_xor_sync(0xffffffffu, vmax[i], o));
+    }
+  }
+  if (!active) return;
+
+  const float fq = static_cast<float>(qmax);
+  const float s_row = __fdiv_rn(amax_row, fq);
+  if (gs == 0 && t == 0) scale[r] = s_row;
+
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int vi = i * T + t;
+    if (vi >= nvec) continue;
+    float amax = amax_row, s = s_row;
+    if (gs != 0) {
+      amax = vmax[i];
+      s = __fdiv_rn(amax, fq);
+      const int g = (vi << 3) / gs;
+      if ((t & ((gs >> 3) - 1)) == 0) scale[r * G + g] = s;
+    }
+    const __half2 *h = reinterpret_cast<const __half2 *>(&v[i]);
+    int qi[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 f = __half22float2(h[j]);
+      qi[2 * j] = quant1(f.x, s, amax, qmax);
+      qi[2 * j + 1] = quant1(f.y, s, amax, qmax);
+    }
+    if (packed == nullptr) {
+      uint32_t lo = (qi[0] & 0xff) | ((qi[1] & 0xff) << 8) |
+                    ((qi[2] & 0xff) << 16) | ((uint32_t)(qi[3] & 0xff) << 24);
+      uint32_t hi = (qi[4] & 0xff) | ((qi[5] & 0xff) << 8) |
+                    ((qi[6] & 0xff) << 16) | ((uint32_t)(qi[7] & 0xff) << 24);
+      reinterpret_cast<uint2 *>(q + r * K)[vi] = make_uint2(lo, hi);
+    } else {
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w |= (uint32_t)(qi[j] & 0xf) << (4 * j);
+      packed[r * (K >> 3) + vi] = w;
+    }
+  }
+}
+
+template <int V>
+int launch_v(const __half *x, long R, int K, int gs, int qmax, int T,
+             int8_t *q, uint8_t *packed, float *scale, cudaStream_t s) {
+  const int block = 256;
+  const int rows_per_block = block / T;
+  const long grid = (R + rows_per_block - 1) / rows_per_block;
+  row_quant_kernel<V><<<static_cast<unsigned>(grid), block, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), R, K, gs, qmax, T, q,
+      reinterpret_cast<uint32_t *>(packed), scale);
+  return launch_status();
+}
+
+}  // namespace
+
+int launch_row_quant(const __half *x, int R, int K, int group_size, int qmax,
+                     int8_t *q, uint8_t *packed, float *scale, cudaStream_t s) {
+  if (R == 0) return W8A8_OK;
+  const int nvec = K >> 3;
+  int T = 32;
+  while (T < 256 && (nvec + T - 1) / T > 16) T <<= 1;
+  const int V = (nvec + T - 1) / T;
+  if (V > 16) return W8A8_ERR_INVALID_ARG;  // K > 32768
+  switch (V) {
+#define W8A8_CASE(n) \
+  case n:            \
+    return launch_v<n>(x, R, K, group_size, qmax, T, q, packed, scale, s);
+    W8A8_CASE(1) W8A8_CASE(2) W8A8_CASE(3) W8A8_CASE(4) W8A8_CASE(5)
+    W8A8_CASE(6) W8A8_CASE(7) W8A8_CASE(8) W8A8_CASE(9) W8A8_CASE(10)
+    W8A8_CASE(11) W8A8_CASE(12) W8A8_CASE(13) W8A8_CASE(14) W8A8_CASE(15)
+    W8A8_CASE(16)
+#undef W8A8_CASE
+    default:
+      return W8A8_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace w8a8
