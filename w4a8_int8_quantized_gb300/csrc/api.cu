@@ -91,7 +91,7 @@ int gemm_dispatch(const int8_t *xq, const float *sa, const void *W,
     return launch_gemv_w8a8(xq, sa, static_cast<const int8_t *>(W), sw, N, K,
                             gs, y, s);
   }
-  return launch_gemm_mma(xq, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
+  return launch_gemm_tc(xq, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
 }
 
 }  // namespace
@@ -232,8 +232,8 @@ int w8a8_gemm_i32(const int8_t *xq, const void *Wq, int M, int N, int K,
   if (M == 0 || N == 0) return W8A8_OK;
   W8A8_TRY(check_ptrs16({xq, Wq, acc}));
   W8A8_TRY(check_device());
-  return launch_gemm_mma(xq, nullptr, Wq, nullptr, M, N, K, group_size, wbits,
-                         nullptr, acc, as_stream(stream));
+  return launch_gemm_tc(xq, nullptr, Wq, nullptr, M, N, K, group_size, wbits,
+                        nullptr, acc, as_stream(stream));
 }
 
 }  // extern "C"

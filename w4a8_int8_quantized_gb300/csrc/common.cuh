@@ -72,8 +72,8 @@ int launch_gemv_w4a8(const int8_t *xq, const float *sa, const uint8_t *Wp,
 
 // GEMMs for M > 1.  acc_out != nullptr exports the exact int32 (per-group)
 // sums [M, N, G] instead of the fp16 output.
-int launch_gemm_mma(const int8_t *xq, const float *sa, const void *W,
-                    const float *sw, int M, int N, int K, int group_size,
-                    int wbits, __half *y, int32_t *acc_out, cudaStream_t s);
+int launch_gemm_tc(const int8_t *xq, const float *sa, const void *W,
+                   const float *sw, int M, int N, int K, int group_size,
+                   int wbits, __half *y, int32_t *acc_out, cudaStream_t s);
 
 }  // namespace w8a8
