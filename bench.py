@@ -285,7 +285,9 @@ def run_ours(args):
     bufs = {}
     for m in MS:
         x = torch.from_numpy(inputs["x"][m]).to(device)
-        xq = torch.empty((m, K_IN), dtype=torch.int8, device=device)
+        # the codes in the format linear() uses: fp16 values for the GEMM
+        # (M > 1), int8 for the matrix-vector kernel (M == 1)
+        xq = torch.empty((m, K_IN), dtype=torch.int8 if m == 1 else torch.float16, device=device)
         sa = torch.empty((m, 1), dtype=torch.float32, device=device)
         y = torch.empty((m, N_OUT), dtype=torch.float16, device=device)
         ws_bytes = w8.w8a8_linear_workspace_bytes(m, K_IN, 0)
@@ -308,16 +310,24 @@ def run_ours(args):
         if st != 0:
             raise RuntimeError(f"{what}: status {st}")
 
+    # the two launches of linear(), called through their own C entry points
+    # so that each is timed on its own
     def call_quant(m):
         b = bufs[m]
-        check(lib.quantize_act_per_token(P(b["x"].data_ptr()), m, K_IN, 0, P(b["xq"].data_ptr()),
-                                         P(b["sa"].data_ptr()), s_ptr), "quantize")
+        f = lib.quantize_act_per_token if m == 1 else lib.quantize_act_per_token_h
+        check(f(P(b["x"].data_ptr()), m, K_IN, 0, P(b["xq"].data_ptr()),
+                P(b["sa"].data_ptr()), s_ptr), "quantize")
 
     def call_gemm(m):
         b = bufs[m]
-        f = lib.w8a8_mv if m == 1 else lib.w8a8_gemm
-        check(f(P(b["xq"].data_ptr()), P(b["sa"].data_ptr()), P(wq.data_ptr()),
-                P(sw.data_ptr()), m, N_OUT, K_IN, 0, P(b["y"].data_ptr()), s_ptr), "gemm")
+        if m == 1:
+            st = lib.w8a8_mv(P(b["xq"].data_ptr()), P(b["sa"].data_ptr()), P(wq.data_ptr()),
+                             P(sw.data_ptr()), m, N_OUT, K_IN, 0, P(b["y"].data_ptr()), s_ptr)
+        else:
+            st = lib.w8a8_gemm_h(P(b["xq"].data_ptr()), P(b["sa"].data_ptr()), P(wq.data_ptr()),
+                                 P(sw.data_ptr()), m, N_OUT, K_IN, 0, 8, P(b["y"].data_ptr()),
+                                 s_ptr)
+        check(st, "gemm")
 
     def call_linear(m, x, y):
         b = bufs[m]
@@ -402,7 +412,7 @@ def run_ours(args):
         d = {"quant_ms": round(q, 5), "gemm_ms": round(g, 5), "ms": round(q + g, 5),
              "TOPS": round(2.0 * m * N_OUT * K_IN / ((q + g) * 1e-3) / 1e12, 3),
              "gemm_TOPS": round(2.0 * m * N_OUT * K_IN / (g * 1e-3) / 1e12, 3),
-             "quant_GBps": round(m * K_IN * 3 + m * 4, 1) / (q * 1e-3) / 1e9}
+             "quant_GBps": (m * K_IN * (3 if m == 1 else 4) + m * 4) / (q * 1e-3) / 1e9}
         if m == 1:
             d["gemv_GBps"] = round((N_OUT * K_IN + N_OUT * 4 + K_IN + 4 + N_OUT * 2)
                                    / (g * 1e-3) / 1e9, 1)
@@ -440,6 +450,53 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_single(args):
+    """One kernel of the path on one workload shape, called `--steps` times
+    after `--warmup` calls, for profilers (ncu captures); prints the mean
+    CUDA-event time per call (with no L2 flush between calls)."""
+    import torch
+
+    import w4a8_int8_quantized_gb300 as w8
+    torch.cuda.set_device(0)
+    w8.load()
+    m, n, k, gs = args.m, args.n, args.k, args.gs
+    x = torch.from_numpy(synth.activations(m, k, seed=0, **WORKLOAD["act"])).cuda()
+    W = torch.from_numpy(synth.weights(n, k, seed=0)).cuda()
+    if args.only == "w4a8":
+        wq, sw = w8.pack_weight_int4(W)
+    else:
+        wq, sw = w8.quantize_weight_int8(W, gs)
+    xq, sa = w8.quantize_act_per_token(x, gs)
+    xqh, sah = w8.quantize_act_per_token_h(x, gs)
+    y = torch.empty((m, n), dtype=torch.float16, device="cuda")
+
+    def call():
+        if args.only == "quant":
+            w8.quantize_act_per_token_h(x, gs, xqh, sah)
+        elif args.only == "quant_i8":
+            w8.quantize_act_per_token(x, gs, xq, sa)
+        elif args.only == "gemm":
+            w8.w8a8_gemm_h(xqh, sah, wq, sw, gs, 8, y)
+        elif args.only == "gemm_i8":
+            w8.w8a8_gemm(xq, sa, wq, sw, gs, y)
+        elif args.only == "w4a8":
+            w8.w8a8_gemm_h(xqh, sah, wq, sw, 0, 4, y)
+        else:
+            w8.linear(x, wq, sw, gs, 4 if args.only == "linear4" else 8, y=y)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"only": args.only, "M": m, "N": n, "K": k, "gs": gs,
+                      "ms_per_call": e0.elapsed_time(e1) / max(1, args.steps)}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -448,7 +505,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU-oracle sample (about 15 s)")
+    ap.add_argument("--only", choices=["quant", "quant_i8", "gemm", "gemm_i8", "w4a8", "linear",
+                                       "linear4"],
+                    help="run one kernel of the path on one shape (for profilers)")
+    ap.add_argument("--m", type=int, default=8192)
+    ap.add_argument("--n", type=int, default=N_OUT)
+    ap.add_argument("--k", type=int, default=K_IN)
+    ap.add_argument("--gs", type=int, default=0)
     args = ap.parse_args()
+    if args.only:
+        run_single(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

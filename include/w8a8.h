@@ -138,14 +138,35 @@ int w4a8_gemm(const int8_t *xq, const float *scale_a, const uint8_t *Wp,
               const float *scale_w, int M, int N, int K, w8a8_half *y,
               w8a8_stream_t stream);
 
+/* quantize_act_per_token with the INT8 codes written as fp16 values (every
+ * code in [-127, 127] is an fp16 integer exactly): the operand format the
+ * tensor-core GEMM reads without converting, which linear() uses for M > 1.
+ *   x        fp16 [M, K]
+ *   xq_h     fp16 [M, K]        (out) the codes q, as fp16
+ *   scale_a  fp32 [M, G]        (out) */
+int quantize_act_per_token_h(const w8a8_half *x, int M, int K, int group_size,
+                             w8a8_half *xq_h, float *scale_a, w8a8_stream_t stream);
+
+/* The GEMM of w8a8_gemm (wbits 8) or w4a8_gemm (wbits 4, group_size 0) with
+ * the activation codes given as fp16 values, as quantize_act_per_token_h
+ * writes them.  Codes outside [-127, 127] or not integral are outside the
+ * contract.  Always the tensor-core GEMM, for any M >= 1.
+ *   xq_h fp16 [M, K], scale_a fp32 [M, G]; Wq int8 [N, K] or packed uint8
+ *   [N, K/2]; scale_w fp32 [N, G]; y fp16 [M, N] (out) */
+int w8a8_gemm_h(const w8a8_half *xq_h, const float *scale_a, const void *Wq,
+                const float *scale_w, int M, int N, int K, int group_size, int wbits,
+                w8a8_half *y, w8a8_stream_t stream);
+
 /* Bytes of workspace that linear() needs for M rows of K activations: the
- * INT8 activations and their fp32 scales, each region 256-byte aligned. */
+ * activation codes (fp16 values for M > 1, INT8 for M == 1) and their fp32
+ * scales, each region 256-byte aligned. */
 size_t w8a8_linear_workspace_bytes(int M, int K, int group_size);
 
 /* The whole layer, CiderLinear's forward ("cider 소개": seq_len > 1 ->
  * INT8 GEMM, seq_len == 1 -> INT8 MV kernel): quantize x per token into
- * the workspace, then run the GEMM (M > 1) or the matrix-vector kernel
- * (M == 1) with the fused dequant.
+ * the workspace (quantize_act_per_token_h for M > 1, quantize_act_per_token
+ * for M == 1), then run the GEMM (w8a8_gemm_h) or the matrix-vector kernel
+ * with the fused dequant.
  *   x        fp16 [M, K]
  *   Wq       int8 [N, K] (wbits 8) or packed uint8 [N, K/2] (wbits 4)
  *   scale_w  fp32 [N, G] (wbits 4 requires group_size 0)

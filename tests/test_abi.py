@@ -45,10 +45,11 @@ def test_status_strings(lib):
 def test_workspace_bytes(lib):
     f = lib.w8a8_linear_workspace_bytes
     # int8 activations then fp32 scales, each region rounded up to 256 bytes
-    assert f(4096, 2560, 0) == 4096 * 2560 + 4096 * 4
+    # codes: fp16 values for M > 1 (the GEMM operand), int8 for M == 1
+    assert f(4096, 2560, 0) == 2 * 4096 * 2560 + 4096 * 4
     assert f(1, 2560, 0) == 2560 + 256
-    assert f(3, 512, 128) == 1536 + 256
-    assert f(4516, 4096, 64) == 4516 * 4096 + ((4516 * 64 * 4 + 255) // 256) * 256
+    assert f(3, 512, 128) == 2 * 1536 + 256
+    assert f(4516, 4096, 64) == 2 * 4516 * 4096 + ((4516 * 64 * 4 + 255) // 256) * 256
     assert f(-1, 16, 0) == 0
     assert f(4, 100, 64) == 0
 
@@ -87,6 +88,11 @@ def test_argument_errors_before_any_launch(lib):
     assert lin(A16, B16, C16, 4, 8, 64, 0, 8, D16, 16, D16, S0) == WS         # too small
     assert lin(A16, B16, C16, 4, 8, 64, 0, 8, ODD, 1 << 20, D16, S0) == WS    # misaligned
     assert lin(A16, B16, C16, 4, 8, 64, 0, 8, NUL, 1 << 20, D16, S0) == WS    # missing
+    gh = lib.w8a8_gemm_h
+    assert gh(A16, C16, B16, C16, 4, 8, 64, 0, 5, D16, S0) == INV      # wbits
+    assert gh(A16, C16, B16, C16, 4, 8, 64, 64, 4, D16, S0) == INV     # W4 per group
+    assert gh(ODD, C16, B16, C16, 4, 8, 64, 0, 8, D16, S0) == MIS
+    assert lib.quantize_act_per_token_h(A16, 4, 40, 0, B16, C16, S0) == MIS
     i32 = lib.w8a8_gemm_i32
     assert i32(A16, B16, 4, 8, 64, 0, 5, C16, S0) == INV
     assert i32(A16, B16, 4, 8, 64, 64, 4, C16, S0) == INV

@@ -86,6 +86,50 @@ def test_act_quant_bit_exact(M, K, gs):
     np.testing.assert_array_equal(host(sa), rs)
 
 
+def _all_fp16_upto(amax):
+    bits = np.arange(0, 0x7C00, dtype=np.uint16)
+    pos = bits.view(np.float16)
+    pos = pos[pos.astype(np.float32) <= np.float32(amax)]
+    return np.concatenate([pos, -pos[1:]])
+
+
+@pytest.mark.parametrize("amax", [127.0, 100.0, 3.140625, 0.0999755859375, 65504.0,
+                                  1000.5, 2.0 ** -20, 6.103515625e-05])
+def test_act_quant_exhaustive_fp16(amax):
+    """Every finite fp16 value up to a fixed absmax, laid out in rows that
+    each contain +-absmax (so every row has the same scale): the GPU's
+    reciprocal fast path with its near-tie fallback must give exactly the
+    codes of one IEEE division and round-half-even, for all of them."""
+    vals = _all_fp16_upto(amax)
+    K = 4096
+    per_row = K - 2
+    rows = -(-vals.size // per_row)
+    x = np.zeros((rows, K), np.float16)
+    flat = np.resize(vals, rows * per_row).reshape(rows, per_row)
+    x[:, 0] = np.float16(amax)
+    x[:, 1] = -np.float16(amax)
+    x[:, 2:] = flat
+    for gs in (0, 128):
+        xq, sa = w8.quantize_act_per_token(dev(x), gs)
+        rq, rs = oracle.quantize_act_per_token(x, gs)
+        np.testing.assert_array_equal(host(xq), rq)
+        np.testing.assert_array_equal(host(sa), rs)
+    xh, sh = w8.quantize_act_per_token_h(dev(x))
+    rq, rs = oracle.quantize_act_per_token(x)
+    np.testing.assert_array_equal(host(xh), rq.astype(np.float16))
+    np.testing.assert_array_equal(host(sh), rs)
+
+
+@pytest.mark.parametrize("M,K,gs", [(3, 48, 0), (130, 2560, 128), (257, 4096, 64), (5, 14336, 0)])
+def test_act_quant_half_codes(M, K, gs):
+    """quantize_act_per_token_h writes exactly the INT8 codes, as fp16."""
+    x = act(M, K, seed=K + 1, zero_rows=(0,), n_outliers=3, outlier_scale=40.0)
+    xh, sa = w8.quantize_act_per_token_h(dev(x), gs)
+    rq, rs = oracle.quantize_act_per_token(x, gs)
+    np.testing.assert_array_equal(host(xh), rq.astype(np.float16))
+    np.testing.assert_array_equal(host(sa), rs)
+
+
 @pytest.mark.parametrize("N,K,gs", [(1, 16, 0), (257, 512, 0), (130, 2560, 64),
                                     (64, 4096, 128), (33, 14336, 0)])
 def test_weight_quant_bit_exact(N, K, gs):
@@ -160,6 +204,27 @@ def test_w8a8_gemm_output(M, N, K, gs):
     wq, sw = oracle.quantize_weight_int8(W, gs)
     ref = oracle.dequant(oracle.int_gemm(xq, wq, gs), sa, sw)
     y = host(w8.w8a8_gemm(dev(xq), dev(sa), dev(wq), dev(sw), gs))
+    assert_fp16_close(y, ref)
+    assert_bits(y, ref)
+
+
+@pytest.mark.parametrize("M,N,K,gs,wbits", [
+    (130, 257, 512, 0, 8), (257, 130, 2560, 0, 8), (1, 300, 2560, 0, 8), (64, 96, 4096, 64, 8),
+    (200, 257, 2560, 128, 8), (2, 3, 16, 0, 8), (129, 520, 14336, 0, 8), (300, 257, 4096, 0, 4),
+    (1, 129, 512, 0, 4)])
+def test_gemm_with_half_codes(M, N, K, gs, wbits):
+    """The GEMM fed with fp16 activation codes (the path linear uses for
+    M > 1) gives the oracle's outputs bit for bit."""
+    x = act(M, K, seed=K + 7, n_outliers=4, outlier_scale=40.0, zero_rows=(M - 1,))
+    W = synth.weights(N, K, seed=N + 7)
+    xq, sa = oracle.quantize_act_per_token(x, gs)
+    if wbits == 8:
+        wq, sw = oracle.quantize_weight_int8(W, gs)
+        ref = oracle.dequant(oracle.int_gemm(xq, wq, gs), sa, sw)
+    else:
+        wq, sw = oracle.pack_weight_int4(W)
+        ref = oracle.dequant(oracle.int_gemm(xq, oracle.unpack_int4(wq, K)), sa, sw)
+    y = host(w8.w8a8_gemm_h(dev(xq.astype(np.float16)), dev(sa), dev(wq), dev(sw), gs, wbits))
     assert_fp16_close(y, ref)
     assert_bits(y, ref)
 

@@ -28,8 +28,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or K",
 # every symbol that include/w8a8.h declares
 EXPORTS = ("w8a8_is_available", "w8a8_status_string", "w8a8_check_status",
            "quantize_weight_int8", "pack_weight_int4", "quantize_act_per_token",
-           "w8a8_gemm", "w8a8_mv", "w4a8_gemm", "w8a8_linear_workspace_bytes",
-           "linear", "w8a8_gemm_i32")
+           "w8a8_gemm", "w8a8_mv", "w4a8_gemm", "quantize_act_per_token_h", "w8a8_gemm_h",
+           "w8a8_linear_workspace_bytes", "linear", "w8a8_gemm_i32")
 
 
 class W8A8Error(RuntimeError):
@@ -60,6 +60,8 @@ def load(path: str | None = None):
             "w8a8_gemm": ([P, P, P, P, I, I, I, I, P, P], I),
             "w8a8_mv": ([P, P, P, P, I, I, I, I, P, P], I),
             "w4a8_gemm": ([P, P, P, P, I, I, I, P, P], I),
+            "quantize_act_per_token_h": ([P, I, I, I, P, P, P], I),
+            "w8a8_gemm_h": ([P, P, P, P, I, I, I, I, I, P, P], I),
             "w8a8_linear_workspace_bytes": ([I, I, I], Z),
             "linear": ([P, P, P, I, I, I, I, I, P, Z, P, P], I),
             "w8a8_gemm_i32": ([P, P, I, I, I, I, I, P, P], I),
@@ -198,6 +200,41 @@ def w4a8_gemm(xq, scale_a, Wp, scale_w, y=None):
     _need(y, torch.float16, "y", (M, N))
     _check(load().w4a8_gemm(_ptr(xq), _ptr(scale_a), _ptr(Wp), _ptr(scale_w), M, N, K,
                             _ptr(y), _stream()), "w4a8_gemm")
+    return y
+
+
+def quantize_act_per_token_h(x: torch.Tensor, group_size: int = 0, xq_h=None, scale_a=None):
+    """fp16 x [M, K] -> (INT8 codes as fp16 xq_h [M, K], fp32 scale_a [M, G])."""
+    _need(x, torch.float16, "x")
+    M, K = x.shape
+    G = _groups(K, group_size)
+    xq_h = torch.empty((M, K), dtype=torch.float16, device=x.device) if xq_h is None else xq_h
+    scale_a = (torch.empty((M, G), dtype=torch.float32, device=x.device)
+               if scale_a is None else scale_a)
+    _need(xq_h, torch.float16, "xq_h", (M, K))
+    _need(scale_a, torch.float32, "scale_a", (M, G))
+    _check(load().quantize_act_per_token_h(_ptr(x), M, K, group_size, _ptr(xq_h),
+                                           _ptr(scale_a), _stream()), "quantize_act_per_token_h")
+    return xq_h, scale_a
+
+
+def w8a8_gemm_h(xq_h, scale_a, Wq, scale_w, group_size: int = 0, wbits: int = 8, y=None):
+    """GEMM with the activation codes given as fp16 values (wbits 8: int8 Wq
+    [N, K]; wbits 4: packed Wq [N, K/2])."""
+    _need(xq_h, torch.float16, "xq_h")
+    M, K = xq_h.shape
+    G = _groups(K, group_size)
+    wdtype = torch.int8 if wbits == 8 else torch.uint8
+    _need(Wq, wdtype, "Wq")
+    N = Wq.shape[0]
+    if Wq.shape[1] * (1 if wbits == 8 else 2) != K:
+        raise ValueError("Wq inner dimension does not match K")
+    _need(scale_a, torch.float32, "scale_a", (M, G))
+    _need(scale_w, torch.float32, "scale_w", (N, G))
+    y = torch.empty((M, N), dtype=torch.float16, device=xq_h.device) if y is None else y
+    _need(y, torch.float16, "y", (M, N))
+    _check(load().w8a8_gemm_h(_ptr(xq_h), _ptr(scale_a), _ptr(Wq), _ptr(scale_w), M, N, K,
+                              group_size, wbits, _ptr(y), _stream()), "w8a8_gemm_h")
     return y
 
 

@@ -91,7 +91,7 @@ int gemm_dispatch(const int8_t *xq, const float *sa, const void *W,
     return launch_gemv_w8a8(xq, sa, static_cast<const int8_t *>(W), sw, N, K,
                             gs, y, s);
   }
-  return launch_gemm_tc(xq, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
+  return launch_gemm_tc(xq, false, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
 }
 
 }  // namespace
@@ -193,10 +193,36 @@ int w4a8_gemm(const int8_t *xq, const float *scale_a, const uint8_t *Wp,
                        reinterpret_cast<__half *>(y), as_stream(stream));
 }
 
+int quantize_act_per_token_h(const w8a8_half *x, int M, int K, int group_size,
+                             w8a8_half *xq_h, float *scale_a, w8a8_stream_t stream) {
+  W8A8_TRY(check_shape(M, 0, K, group_size, 16));
+  if (M == 0) return W8A8_OK;
+  W8A8_TRY(check_ptrs16({x, xq_h}));
+  W8A8_TRY(check_ptrs4({scale_a}));
+  W8A8_TRY(check_device());
+  return launch_row_quant_half(reinterpret_cast<const __half *>(x), M, K, group_size,
+                               reinterpret_cast<__half *>(xq_h), scale_a, as_stream(stream));
+}
+
+int w8a8_gemm_h(const w8a8_half *xq_h, const float *scale_a, const void *Wq,
+                const float *scale_w, int M, int N, int K, int group_size, int wbits,
+                w8a8_half *y, w8a8_stream_t stream) {
+  if (wbits != 8 && wbits != 4) return W8A8_ERR_INVALID_ARG;
+  if (wbits == 4 && group_size != 0) return W8A8_ERR_INVALID_ARG;
+  W8A8_TRY(check_shape(M, N, K, group_size, wbits == 4 ? 32 : 16));
+  if (M == 0 || N == 0) return W8A8_OK;
+  W8A8_TRY(check_ptrs16({xq_h, Wq, y}));
+  W8A8_TRY(check_ptrs4({scale_a, scale_w}));
+  W8A8_TRY(check_device());
+  return launch_gemm_tc(xq_h, true, scale_a, Wq, scale_w, M, N, K, group_size, wbits,
+                        reinterpret_cast<__half *>(y), nullptr, as_stream(stream));
+}
+
 size_t w8a8_linear_workspace_bytes(int M, int K, int group_size) {
   if (M < 0 || K <= 0 || !valid_group_size(K, group_size)) return 0;
   const size_t G = static_cast<size_t>(groups_of(K, group_size));
-  return round256(static_cast<size_t>(M) * K) +
+  const size_t code_bytes = M > 1 ? 2 : 1;  // fp16 codes for the GEMM, int8 for the MV
+  return round256(static_cast<size_t>(M) * K * code_bytes) +
          round256(static_cast<size_t>(M) * G * sizeof(float));
 }
 
@@ -214,13 +240,21 @@ int linear(const w8a8_half *x, const void *Wq, const float *scale_w, int M,
     return W8A8_ERR_WORKSPACE;
   W8A8_TRY(check_device());
   cudaStream_t s = as_stream(stream);
-  int8_t *xq = static_cast<int8_t *>(workspace);
+  const size_t code_bytes = M > 1 ? 2 : 1;
   float *sa = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                        round256(static_cast<size_t>(M) * K));
-  W8A8_TRY(launch_row_quant(reinterpret_cast<const __half *>(x), M, K,
-                            group_size, 127, xq, nullptr, sa, s));
-  return gemm_dispatch(xq, sa, Wq, scale_w, M, N, K, group_size, wbits,
-                       reinterpret_cast<__half *>(y), s);
+                                        round256(static_cast<size_t>(M) * K * code_bytes));
+  if (M == 1) {
+    int8_t *xq = static_cast<int8_t *>(workspace);
+    W8A8_TRY(launch_row_quant(reinterpret_cast<const __half *>(x), M, K, group_size, 127, xq,
+                              nullptr, sa, s));
+    return gemm_dispatch(xq, sa, Wq, scale_w, M, N, K, group_size, wbits,
+                         reinterpret_cast<__half *>(y), s);
+  }
+  __half *xq_h = static_cast<__half *>(workspace);
+  W8A8_TRY(launch_row_quant_half(reinterpret_cast<const __half *>(x), M, K, group_size, xq_h,
+                                 sa, s));
+  return launch_gemm_tc(xq_h, true, sa, Wq, scale_w, M, N, K, group_size, wbits,
+                        reinterpret_cast<__half *>(y), nullptr, s);
 }
 
 int w8a8_gemm_i32(const int8_t *xq, const void *Wq, int M, int N, int K,
@@ -232,7 +266,7 @@ int w8a8_gemm_i32(const int8_t *xq, const void *Wq, int M, int N, int K,
   if (M == 0 || N == 0) return W8A8_OK;
   W8A8_TRY(check_ptrs16({xq, Wq, acc}));
   W8A8_TRY(check_device());
-  return launch_gemm_tc(xq, nullptr, Wq, nullptr, M, N, K, group_size, wbits,
+  return launch_gemm_tc(xq, false, nullptr, Wq, nullptr, M, N, K, group_size, wbits,
                         nullptr, acc, as_stream(stream));
 }
 

@@ -70,10 +70,15 @@ int launch_gemv_w8a8(const int8_t *xq, const float *sa, const int8_t *Wq,
 int launch_gemv_w4a8(const int8_t *xq, const float *sa, const uint8_t *Wp,
                      const float *sw, int N, int K, __half *y, cudaStream_t s);
 
-// GEMMs for M > 1.  acc_out != nullptr exports the exact int32 (per-group)
-// sums [M, N, G] instead of the fp16 output.
-int launch_gemm_tc(const int8_t *xq, const float *sa, const void *W,
-                   const float *sw, int M, int N, int K, int group_size,
-                   int wbits, __half *y, int32_t *acc_out, cudaStream_t s);
+// Row quantization writing the INT8 codes as fp16 values.
+int launch_row_quant_half(const __half *x, int R, int K, int group_size, __half *qh,
+                          float *scale, cudaStream_t s);
+
+// Tensor-core GEMM.  A is int8 codes [M, K] (a_half false) or the same codes
+// as fp16 values (a_half true).  acc_out != nullptr exports the exact int32
+// (per-group) sums [M, N, G] instead of the fp16 output.
+int launch_gemm_tc(const void *A, bool a_half, const float *sa, const void *W,
+                   const float *sw, int M, int N, int K, int group_size, int wbits,
+                   __half *y, int32_t *acc_out, cudaStream_t s);
 
 }  // namespace w8a8

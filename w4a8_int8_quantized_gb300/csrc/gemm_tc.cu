@@ -19,17 +19,28 @@
 //     it to an int32 running sum in registers.  Per-group scales drain at
 //     every group (64 or 128 of K) and rescale each exact partial in fp32.
 //
-// Kernel layout (persistent, one CTA of 16 warps per SM, 128 x 256 output
-// tiles, 64-deep K blocks):
-//   warp 0      TMA producer: INT8 (or packed INT4) A / B tiles into a
-//               4-stage staging ring in shared memory;
+// Operand roles: the weights are the MMA's A operand (128 output channels
+// per tile, the TMEM lanes) and the activations its B operand (BT = 256 or
+// 128 tokens per tile, the TMEM columns), so the operand that has to be
+// converted from INT8 / INT4 codes to fp16 in shared memory is the smaller
+// 128-row one.  The activations arrive either as fp16 codes, which TMA
+// places directly in the MMA's layout, or as INT8 codes, converted too.
+//
+// Kernel layout (persistent, one CTA of 16 warps per SM, 64-deep K blocks):
+//   warp 0      TMA producer: INT8 / packed INT4 weight tiles into a staging
+//               ring; activation tiles into the staging ring (INT8) or
+//               straight into the MMA operand stage (fp16 codes, 128-byte
+//               swizzle, K-major);
 //   warp 1      allocates TMEM and issues the MMAs (one thread): four
-//               128x256x16 tcgen05.mma per K block into one of two TMEM
+//               128 x BT x 16 tcgen05.mma per K block into one of two TMEM
 //               accumulators (ping-pong per chunk);
 //   warps 2-7   converters: INT8 / INT4 codes -> fp16, written in the
-//               128-byte-swizzled K-major layout the MMA reads (2 stages);
+//               128-byte-swizzled K-major layout the MMA reads;
 //   warps 8-15  epilogue: drain TMEM (tcgen05.ld), exact int32 sums or fp32
-//               per-group rescale, then the fp16 output.
+//               per-group rescale, then the fp16 output; each thread owns
+//               one output channel and BT / 2 tokens, so a warp's store
+//               writes 32 consecutive channels of one token.  The
+//               activation scales of the tile are staged in shared memory.
 // Stages hand over through mbarriers; every wait is bounded, and a wait that
 // gives up records a code in the device error word, raises an abort flag
 // seen by every role, lets in-flight copies and MMAs land, frees TMEM and
@@ -41,32 +52,45 @@
 namespace w8a8 {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int S8 = 4, S16 = 2;
+constexpr int BW = 128, BK = 64;  // weight rows (output channels) per tile, K block
+constexpr int S8 = 3;             // staging ring depth
 constexpr int NUM_THREADS = 512;
 constexpr int CONV_WARPS = 6, EPI_WARPS = 8;
-constexpr int A8_BYTES = BM * BK;        // INT8 A stage
-constexpr int B8_BYTES = BN * BK;        // INT8 B stage (packed INT4 uses half)
-constexpr int A16_BYTES = BM * BK * 2;   // fp16 A stage, 128-byte rows
-constexpr int B16_BYTES = BN * BK * 2;   // fp16 B stage
-constexpr int OFF_A8 = 0;
-constexpr int OFF_B8 = OFF_A8 + S8 * A8_BYTES;
-constexpr int OFF_A16 = OFF_B8 + S8 * B8_BYTES;
-constexpr int OFF_B16 = OFF_A16 + S16 * A16_BYTES;
-constexpr int OFF_BAR = OFF_B16 + S16 * B16_BYTES;
-constexpr int NUM_BARS = 2 * S8 + 2 * S16 + 2 + 2 + 1;
-constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + alignment slack
-constexpr uint32_t TMEM_COLS = 512;
+constexpr int CONV_THREADS = CONV_WARPS * 32, EPI_THREADS = EPI_WARPS * 32;
 constexpr long long kTimeoutCycles = 4000000000LL;  // about 2 s at 2 GHz
 
+// Shared-memory plan.  XH: activations arrive as fp16 codes (TMA straight
+// into the operand stage, no activation staging); BT: tokens per tile.
+template <bool XH, int BT>
+struct Plan {
+  static constexpr int W8_BYTES = BW * BK;         // INT8 weight stage (INT4 uses half)
+  static constexpr int X8_BYTES = XH ? 0 : BT * BK;
+  static constexpr int W16_BYTES = BW * BK * 2;    // fp16 operand stages, 128-byte rows
+  static constexpr int X16_BYTES = BT * BK * 2;
+  static constexpr int S16 = XH ? 4 : 3;
+  static constexpr int OFF_W8 = 0;
+  static constexpr int OFF_X8 = OFF_W8 + S8 * W8_BYTES;
+  static constexpr int OFF_W16 = OFF_X8 + S8 * X8_BYTES;
+  static constexpr int OFF_X16 = OFF_W16 + S16 * W16_BYTES;
+  static constexpr int OFF_SA = OFF_X16 + S16 * X16_BYTES;   // 2 x BT fp32 scales
+  static constexpr int OFF_BAR = OFF_SA + 2 * BT * 4;
+  static constexpr int NUM_BARS = 2 * S8 + 2 * S16 + 2 + 2 + 2 + 1;
+  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + align slack
+  static constexpr uint32_t TMEM_COLS = 2 * BT;  // two accumulators of BT fp32 columns
+};
+static_assert(Plan<true, 256>::SMEM_BYTES <= 232448, "shared memory plan too large");
+static_assert(Plan<false, 256>::SMEM_BYTES <= 232448, "shared memory plan too large");
+
 // instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
-// N = 256, M = 128
-constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) |
-                           (static_cast<uint32_t>(BN >> 3) << 17) |
-                           (static_cast<uint32_t>(BM >> 4) << 24);
+// M = 128 (weights), N = BT (tokens)
+template <int BT>
+__host__ __device__ constexpr uint32_t idesc() {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BT >> 3) << 17) |
+         (static_cast<uint32_t>(BW >> 4) << 24);
+}
 
 struct TcParams {
-  int M, N, K, gs, G, nkb, chunk_kb, mblocks, ntiles;
+  int M, N, K, gs, G, nkb, chunk_kb, nblocks, ntiles;
   const float *sa;
   const float *sw;
   __half *y;
@@ -134,11 +158,11 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accum) {
+                                       uint32_t idesc, uint32_t accum) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accum));
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
 }
 
 // shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -153,22 +177,33 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   return d;
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+// 32 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
         "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
-        "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),
+        "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+        "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
 }
 
-// Ordered global accesses for the epilogue: as volatile asm they keep their
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Ordered memory accesses for the epilogue: as volatile asm they keep their
 // program order, so a fully unrolled loop does not hoist all of its loads
 // ahead of its stores (which would need one register per load).
-__device__ __forceinline__ float ldg_f32(const float *ptr) {
-  float v;
-  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
   return v;
 }
 
@@ -182,12 +217,14 @@ __device__ __forceinline__ void stg_b16(void *ptr, __half v) {
   asm volatile("st.global.b16 [%0], %1;" ::"l"(ptr), "h"(__half_as_ushort(v)) : "memory");
 }
 
-__device__ __forceinline__ void stg_b32(void *ptr, int v) {
-  asm volatile("st.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+__device__ __forceinline__ float ldg_f32(const float *ptr) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+  return v;
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+__device__ __forceinline__ void stg_b32(void *ptr, int v) {
+  asm volatile("st.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
 // Bounded wait.  Returns false if the CTA is aborting or the wait gave up
@@ -231,6 +268,13 @@ __device__ __forceinline__ void i8x4_to_h(uint32_t w, uint32_t &h01, uint32_t &h
   h23 = *reinterpret_cast<uint32_t *>(&b);
 }
 
+__device__ __forceinline__ uint4 i8x8_to_h(uint2 v) {
+  uint4 o;
+  i8x4_to_h(v.x, o.x, o.y);
+  i8x4_to_h(v.y, o.z, o.w);
+  return o;
+}
+
 // 8 two's-complement nibbles (element 2i in the low nibble of byte i) -> 8
 // fp16 in element order: a nibble v becomes 1024 + (v + 8), minus 1032.
 __device__ __forceinline__ uint4 i4x8_to_h(uint32_t w) {
@@ -254,27 +298,66 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int j) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
 }
 
+// Converts `rows` rows x 64 codes of a staged tile into the swizzled fp16
+// operand tile; unit u = (row u / 8, 8-element group u % 8).  Four units per
+// thread are loaded before any is converted, for memory-level parallelism.
+template <bool INT4>
+__device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, int rows,
+                                             int ct) {
+  const int units = rows * 8;
+#pragma unroll 1
+  for (int u0 = ct; u0 < units; u0 += 4 * CONV_THREADS) {
+    uint2 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int u = u0 + i * CONV_THREADS;
+      v[i] = make_uint2(0, 0);
+      if (u < units) {
+        const int r = u >> 3, j = u & 7;
+        if (INT4) {
+          v[i].x = *reinterpret_cast<const uint32_t *>(src + r * 32 + j * 4);
+        } else {
+          v[i] = *reinterpret_cast<const uint2 *>(src + r * 64 + j * 8);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int u = u0 + i * CONV_THREADS;
+      if (u < units) {
+        const int r = u >> 3, j = u & 7;
+        const uint4 o = INT4 ? i4x8_to_h(v[i].x) : i8x8_to_h(v[i]);
+        *reinterpret_cast<uint4 *>(dst + sw128_off(r, j)) = o;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------- kernel ----
 
-template <int WBITS, bool PERGROUP>
+template <int WBITS, bool PERGROUP, bool XH, int BT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                   const __grid_constant__ CUtensorMap tmW, const TcParams p) {
+  using PL = Plan<XH, BT>;
+  constexpr int S16 = PL::S16;
+  constexpr int CPT = BT / 2;  // token columns per epilogue thread
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *sm = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const uint32_t bar0 = base + OFF_BAR;
+  const uint32_t bar0 = base + PL::OFF_BAR;
   auto full8 = [&](int s) { return bar0 + 8u * s; };
   auto empty8 = [&](int s) { return bar0 + 8u * (S8 + s); };
   auto full16 = [&](int s) { return bar0 + 8u * (2 * S8 + s); };
   auto empty16 = [&](int s) { return bar0 + 8u * (2 * S8 + S16 + s); };
   auto accfull = [&](int r) { return bar0 + 8u * (2 * S8 + 2 * S16 + r); };
   auto accempty = [&](int r) { return bar0 + 8u * (2 * S8 + 2 * S16 + 2 + r); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * S8 + 2 * S16 + 4);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + NUM_BARS * 8);
+  auto saready = [&](int b) { return bar0 + 8u * (2 * S8 + 2 * S16 + 4 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S8 + 2 * S16 + 6);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + PL::OFF_BAR + PL::NUM_BARS * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
@@ -283,25 +366,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(empty8(s), CONV_WARPS);
     }
     for (int s = 0; s < S16; ++s) {
-      mbar_init(full16(s), CONV_WARPS);
+      mbar_init(full16(s), CONV_WARPS + (XH ? 1 : 0));
       mbar_init(empty16(s), 1);
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(accfull(r), 1);
       mbar_init(accempty(r), EPI_WARPS);
+      mbar_init(saready(r), EPI_THREADS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0 && lane == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS));
+                 "r"(PL::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -320,52 +404,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
     // ------------------------------------------------------ epilogue ----
     const int q = warp & 3;             // TMEM lane quadrant of this warp
-    const int half = (warp - 8) >> 2;   // which 128 of the 256 columns
-    const int row = q * 32 + lane;
+    const int et = (warp - 8) * 32 + lane;
+    const int half = (warp - 8) >> 2;   // which half of the BT token columns
     const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t cc = 0;
+    const uint32_t sas = base + PL::OFF_SA;
+    float *sas_ptr = reinterpret_cast<float *>(sm + PL::OFF_SA);
+    const bool want_y = p.acc_out == nullptr;
+    uint32_t cc = 0, su = 0;  // chunks drained, scale buffers used
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
-      const int mb = tile % p.mblocks, nb = tile / p.mblocks;
-      const long m = static_cast<long>(mb) * BM + row;
-      const long n0 = static_cast<long>(nb) * BN + half * 128;
-      uint32_t acc[128];  // int32 sums (per channel) or fp32 totals (per group)
+      const int nb = tile % p.nblocks, tb = tile / p.nblocks;
+      const long n = static_cast<long>(nb) * BW + q * 32 + lane;  // this thread's channel
+      const long mtile = static_cast<long>(tb) * BT;
+      const long m0 = mtile + half * CPT;                           // its first token
+      // per channel: stage the tile's BT activation scales now, used at the end
+      uint32_t sb = 0, sph = 0;
+      float swn = 0.f;
+      if (!PERGROUP && want_y) {
+        sb = su & 1u;
+        sph = (su >> 1) & 1u;
+        ++su;
+        if (et < BT) {
+          const long m = mtile + et;
+          sas_ptr[sb * BT + et] = m < p.M ? __ldg(p.sa + m) : 0.f;
+        }
+        mbar_arrive(saready(sb));
+        if (n < p.N) swn = __ldg(p.sw + n);
+      }
+      uint32_t acc[CPT];  // int32 sums (per channel) or fp32 totals (per group)
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0u;
+      for (int i = 0; i < CPT; ++i) acc[i] = 0u;
       const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
       for (int c = 0; c < nchunks; ++c) {
         const uint32_t r = cc & 1u;
+        float sw_g = 0.f;
+        uint32_t gb = 0, gph = 0;
+        if (PERGROUP && want_y) {
+          // stage group c's activation scales for the BT tokens
+          gb = su & 1u;
+          gph = (su >> 1) & 1u;
+          ++su;
+          if (et < BT) {
+            const long m = mtile + et;
+            sas_ptr[gb * BT + et] = m < p.M ? __ldg(p.sa + m * p.G + c) : 0.f;
+          }
+          mbar_arrive(saready(gb));
+          if (n < p.N) sw_g = __ldg(p.sw + n * p.G + c);
+        }
         bool w = wait_bar(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err);
+        if (PERGROUP && want_y)
+          w = w && wait_bar(saready(gb), gph, abort_flag, kDevErrAccumBarrier, p.err);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float sa_g = 0.f;
-        if (PERGROUP && p.acc_out == nullptr && m < p.M) sa_g = p.sa[m * p.G + c];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t v[16];
-          tmem_ld16(tq + r * BN + half * 128 + j * 16, v);
+        for (int j = 0; j < CPT / 32; ++j) {
+          uint32_t v[32];
+          tmem_ld32(tq + r * BT + half * CPT + j * 32, v);
           tmem_wait_ld();
+          if (PERGROUP) {
+            if (want_y) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float f = __uint_as_float(v[i]);
-            const int idx = j * 16 + i;
-            if (PERGROUP) {
-              const long n = n0 + idx;
-              if (p.acc_out != nullptr) {
-                if (m < p.M && n < p.N)
-                  stg_b32(p.acc_out + (m * p.N + n) * p.G + c, __float2int_rn(f));
-              } else {
-                const float swv = n < p.N ? ldg_f32(p.sw + n * p.G + c) : 0.f;
-                acc[idx] = __float_as_uint(__fadd_rn(__uint_as_float(acc[idx]),
-                                                     __fmul_rn(f, __fmul_rn(sa_g, swv))));
+              for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 s4 =
+                    lds_f32x4(sas + (gb * BT + half * CPT + j * 32 + i4 * 4) * 4);
+                const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int idx = j * 32 + i4 * 4 + e;
+                  // (s_a * s_w) first, as in the dequant rule
+                  acc[idx] = __float_as_uint(
+                      __fadd_rn(__uint_as_float(acc[idx]),
+                                __fmul_rn(__uint_as_float(v[i4 * 4 + e]), __fmul_rn(sv[e], sw_g))));
+                  asm volatile("" : "+r"(acc[idx]));  // before the next scale load
+                }
               }
-            } else {
-              acc[idx] = static_cast<uint32_t>(static_cast<int>(acc[idx]) + __float2int_rn(f));
+            } else if (n < p.N) {
+              // export of the exact group partials; sequential addresses
+              int32_t *ap = p.acc_out + ((m0 + j * 32) * p.N + n) * p.G + c;
+              const long step = static_cast<long>(p.N) * p.G;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                if (m0 + j * 32 + i < p.M) stg_b32(ap, __float2int_rn(__uint_as_float(v[i])));
+                ap += step;
+                asm volatile("" : "+l"(ap));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int idx = j * 32 + i;
+              acc[idx] = static_cast<uint32_t>(static_cast<int>(acc[idx]) +
+                                               __float2int_rn(__uint_as_float(v[i])));
             }
           }
+          // finish this slice before the next TMEM load (keeps one slice live)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(acc[j * 32 + i]));
         }
         tc_fence_before();
         __syncwarp();
@@ -373,47 +510,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++cc;
       }
       if (!ok) break;
-      if (m >= p.M) continue;
-      if (p.acc_out != nullptr) {
-        if (!PERGROUP) {
+      if (!want_y) {
+        if (!PERGROUP && n < p.N) {
+          int32_t *ap = p.acc_out + m0 * p.N + n;
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (n0 + i < p.N) stg_b32(p.acc_out + m * p.N + n0 + i, static_cast<int>(acc[i]));
+          for (int i = 0; i < CPT; ++i) {
+            if (m0 + i < p.M) stg_b32(ap, static_cast<int>(acc[i]));
+            ap += p.N;
+            asm volatile("" : "+l"(ap));
+          }
         }
         continue;
       }
-      const float sam = PERGROUP ? 0.f : p.sa[m];
-      __half *yr = p.y + m * p.N;
-      const bool vec = (p.N & 7) == 0;
+      if (!PERGROUP) {
+        bool w = wait_bar(saready(sb), sph, abort_flag, kDevErrAccumBarrier, p.err);
+        if (!__all_sync(0xffffffffu, w)) break;
+      }
+      if (n >= p.N) continue;
+      // y[m, n] for this thread's channel n and tokens m0 .. m0 + CPT - 1: a
+      // warp store covers 32 consecutive channels (64 contiguous bytes).  The
+      // row pointer advances by N per token; the empty asm keeps the compiler
+      // from precomputing all CPT addresses at once.
+      __half *yp = p.y + m0 * p.N + n;
+      const int mcount = static_cast<int>(min(static_cast<long>(CPT), p.M - m0));
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const long nb8 = n0 + c8 * 8;
-        float o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int idx = c8 * 8 + i;
-          if (PERGROUP) {
-            o[i] = __uint_as_float(acc[idx]);
-          } else {
-            const long n = nb8 + i;
-            const float swv = n < p.N ? ldg_f32(p.sw + n) : 0.f;
-            o[i] = __fmul_rn(static_cast<float>(static_cast<int>(acc[idx])),
-                             __fmul_rn(sam, swv));
-          }
+      for (int i4 = 0; i4 < CPT / 4; ++i4) {
+        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!PERGROUP) {
+          const float4 s4 = lds_f32x4(sas + (sb * BT + half * CPT + i4 * 4) * 4);
+          sv[0] = s4.x;
+          sv[1] = s4.y;
+          sv[2] = s4.z;
+          sv[3] = s4.w;
         }
-        if (vec && nb8 + 8 <= p.N) {
-          uint4 h;
-          __half2 t0 = __floats2half2_rn(o[0], o[1]), t1 = __floats2half2_rn(o[2], o[3]);
-          __half2 t2 = __floats2half2_rn(o[4], o[5]), t3 = __floats2half2_rn(o[6], o[7]);
-          h.x = *reinterpret_cast<uint32_t *>(&t0);
-          h.y = *reinterpret_cast<uint32_t *>(&t1);
-          h.z = *reinterpret_cast<uint32_t *>(&t2);
-          h.w = *reinterpret_cast<uint32_t *>(&t3);
-          stg_v4(yr + nb8, h);
-        } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (nb8 + i < p.N) stg_b16(yr + nb8 + i, __float2half_rn(o[i]));
+        for (int e = 0; e < 4; ++e) {
+          const int i = i4 * 4 + e;
+          if (i < mcount) {
+            const float o =
+                PERGROUP ? __uint_as_float(acc[i])
+                         : __fmul_rn(static_cast<float>(static_cast<int>(acc[i])),
+                                     __fmul_rn(sv[e], swn));
+            stg_b16(yp, __float2half_rn(o));
+          }
+          yp += p.N;
+          asm volatile("" : "+l"(yp));
         }
       }
     }
@@ -423,34 +564,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
       // ---------------------------------------------------- TMA producer --
       if (lane == 0) {
-        int s = 0;
-        uint32_t ph = 0;
-        uint32_t pending = 0, pend_ph = 0;  // bit i: stage i issued / its parity
-        const uint32_t bytes = A8_BYTES + (WBITS == 8 ? B8_BYTES : B8_BYTES / 2);
-        for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
-          const int mb = tile % p.mblocks, nb = tile / p.mblocks;
-          bool ok = true;
+        int s8 = 0, s16 = 0;
+        uint32_t ph8 = 0, ph16 = 0;
+        // bit i: stage i has a copy issued / the parity of its phase
+        uint32_t pend8 = 0, pph8 = 0, pend16 = 0, pph16 = 0;
+        const uint32_t bytes8 = (WBITS == 8 ? PL::W8_BYTES : PL::W8_BYTES / 2) + PL::X8_BYTES;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
+          const int nb = tile % p.nblocks, tb = tile / p.nblocks;
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bar(empty8(s), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
+            if (!wait_bar(empty8(s8), ph8 ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full8(s), bytes);
-            tma_load_2d(base + OFF_A8 + s * A8_BYTES, &tmA, full8(s), kb * BK, mb * BM);
-            tma_load_2d(base + OFF_B8 + s * B8_BYTES, &tmB, full8(s),
-                        WBITS == 8 ? kb * BK : kb * (BK / 2), nb * BN);
-            pending |= 1u << s;
-            pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
-            if (++s == S8) {
-              s = 0;
-              ph ^= 1u;
+            mbar_arrive_expect_tx(full8(s8), bytes8);
+            tma_load_2d(base + PL::OFF_W8 + s8 * PL::W8_BYTES, &tmW, full8(s8),
+                        WBITS == 8 ? kb * BK : kb * (BK / 2), nb * BW);
+            if (!XH)
+              tma_load_2d(base + PL::OFF_X8 + s8 * PL::X8_BYTES, &tmX, full8(s8), kb * BK, tb * BT);
+            pend8 |= 1u << s8;
+            pph8 = (pph8 & ~(1u << s8)) | (ph8 << s8);
+            if (++s8 == S8) {
+              s8 = 0;
+              ph8 ^= 1u;
+            }
+            if (XH) {
+              // fp16 activation codes go straight into the MMA operand stage
+              if (!wait_bar(empty16(s16), ph16 ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(full16(s16), PL::X16_BYTES);
+              tma_load_2d(base + PL::OFF_X16 + s16 * PL::X16_BYTES, &tmX, full16(s16), kb * BK,
+                          tb * BT);
+              pend16 |= 1u << s16;
+              pph16 = (pph16 & ~(1u << s16)) | (ph16 << s16);
+              if (++s16 == S16) {
+                s16 = 0;
+                ph16 ^= 1u;
+              }
             }
           }
-          if (!ok) break;
         }
         // every copy this thread issued has landed before the CTA can exit
         for (int i = 0; i < S8; ++i)
-          if ((pending >> i) & 1u) wait_bar_teardown(full8(i), (pend_ph >> i) & 1u);
+          if ((pend8 >> i) & 1u) wait_bar_teardown(full8(i), (pph8 >> i) & 1u);
+        for (int i = 0; i < S16; ++i)
+          if ((pend16 >> i) & 1u) wait_bar_teardown(full16(i), (pph16 >> i) & 1u);
       }
     } else if (warp == 1) {
       // ---------------------------------------------------- MMA issuer ----
@@ -475,12 +635,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t d = tmem + r * BN;
-            const uint32_t a_base = base + OFF_A16 + s * A16_BYTES;
-            const uint32_t b_base = base + OFF_B16 + s * B16_BYTES;
+            const uint32_t d = tmem + r * BT;
+            const uint32_t w_base = base + PL::OFF_W16 + s * PL::W16_BYTES;
+            const uint32_t x_base = base + PL::OFF_X16 + s * PL::X16_BYTES;
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              tc_mma(d, sw128_desc(a_base + k * 32), sw128_desc(b_base + k * 32),
+              tc_mma(d, sw128_desc(w_base + k * 32), sw128_desc(x_base + k * 32), idesc<BT>(),
                      (first && k == 0) ? 0u : 1u);
             }
             tc_commit(empty16(s));
@@ -498,7 +658,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_commit(drain_bar);
         wait_bar_teardown(drain_bar, 0);
       }
-    } else if (warp < 2 + CONV_WARPS) {
+    } else {
       // ---------------------------------------------------- converters ----
       const int ct = (warp - 2) * 32 + lane;
       int s8 = 0, s16 = 0;
@@ -512,34 +672,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          const uint8_t *a8 = sm + OFF_A8 + s8 * A8_BYTES;
-          const uint8_t *b8 = sm + OFF_B8 + s8 * B8_BYTES;
-          uint8_t *a16 = sm + OFF_A16 + s16 * A16_BYTES;
-          uint8_t *b16 = sm + OFF_B16 + s16 * B16_BYTES;
-          // A: 128 rows x 8 units of 8 elements
-#pragma unroll 1
-          for (int u = ct; u < BM * 8; u += CONV_WARPS * 32) {
-            const int r = u >> 3, j = u & 7;
-            const uint2 v = *reinterpret_cast<const uint2 *>(a8 + r * 64 + j * 8);
-            uint4 o;
-            i8x4_to_h(v.x, o.x, o.y);
-            i8x4_to_h(v.y, o.z, o.w);
-            *reinterpret_cast<uint4 *>(a16 + sw128_off(r, j)) = o;
-          }
-          // B: 256 rows x 8 units
-#pragma unroll 1
-          for (int u = ct; u < BN * 8; u += CONV_WARPS * 32) {
-            const int r = u >> 3, j = u & 7;
-            uint4 o;
-            if (WBITS == 8) {
-              const uint2 v = *reinterpret_cast<const uint2 *>(b8 + r * 64 + j * 8);
-              i8x4_to_h(v.x, o.x, o.y);
-              i8x4_to_h(v.y, o.z, o.w);
-            } else {
-              o = i4x8_to_h(*reinterpret_cast<const uint32_t *>(b8 + r * 32 + j * 4));
-            }
-            *reinterpret_cast<uint4 *>(b16 + sw128_off(r, j)) = o;
-          }
+          convert_tile<WBITS == 4>(sm + PL::OFF_W8 + s8 * PL::W8_BYTES,
+                                   sm + PL::OFF_W16 + s16 * PL::W16_BYTES, BW, ct);
+          if (!XH)
+            convert_tile<false>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES,
+                                sm + PL::OFF_X16 + s16 * PL::X16_BYTES, BT, ct);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
@@ -565,7 +702,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(TMEM_COLS));
+                 "r"(PL::TMEM_COLS));
   }
 }
 
@@ -592,52 +729,67 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D UINT8 tensor map over a row-major [rows, cols] byte matrix with a
-// box of [box_rows, box_cols] (no swizzle; out-of-range elements read 0).
-bool make_map(CUtensorMap *map, const void *ptr, long rows, long cols, int box_rows,
-              int box_cols) {
+// 2-D tensor map over a row-major [rows, cols] matrix of 1- or 2-byte
+// elements, box [box_rows, box_cols]; out-of-range elements read 0.  2-byte
+// maps use the 128-byte swizzle (box rows of exactly 128 bytes): the
+// K-major layout the MMA reads.
+bool make_map(CUtensorMap *map, const void *ptr, long rows, long cols, int elem_bytes,
+              int box_rows, int box_cols) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+  const bool h = elem_bytes == 2;
+  return enc(map, h ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+             const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             h ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int WBITS, bool PERGROUP>
-int launch_t(const CUtensorMap &ta, const CUtensorMap &tb, const TcParams &p, cudaStream_t s) {
+template <int WBITS, bool PERGROUP, bool XH, int BT>
+int launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, cudaStream_t s) {
   static bool attr_set[64] = {};
   static int sms[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return W8A8_ERR_CUDA;
+  constexpr int smem = Plan<XH, BT>::SMEM_BYTES;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<WBITS, PERGROUP>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_tc_kernel<WBITS, PERGROUP, XH, BT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return W8A8_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return W8A8_ERR_CUDA;
     attr_set[dev] = true;
   }
   const int grid = p.ntiles < sms[dev] ? p.ntiles : sms[dev];
-  gemm_tc_kernel<WBITS, PERGROUP><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, p);
+  gemm_tc_kernel<WBITS, PERGROUP, XH, BT><<<grid, NUM_THREADS, smem, s>>>(tx, tw, p);
   return launch_status();
+}
+
+template <bool XH, int BT>
+int launch_modes(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, int wbits,
+                 cudaStream_t s) {
+  if (wbits == 4) return launch_t<4, false, XH, BT>(tx, tw, p, s);
+  if (p.gs != 0) return launch_t<8, true, XH, BT>(tx, tw, p, s);
+  return launch_t<8, false, XH, BT>(tx, tw, p, s);
 }
 
 }  // namespace
 
-int launch_gemm_tc(const int8_t *xq, const float *sa, const void *W, const float *sw, int M,
-                   int N, int K, int group_size, int wbits, __half *y, int32_t *acc_out,
-                   cudaStream_t s) {
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, xq, M, K, BM, BK)) return W8A8_ERR_CUDA;
+// X (activations) is int8 codes [M, K] (x_half false) or the same codes as
+// fp16 values (x_half true).  128-token tiles when M <= 128, else 256.
+int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, const float *sw,
+                   int M, int N, int K, int group_size, int wbits, __half *y,
+                   int32_t *acc_out, cudaStream_t s) {
+  const int bt = M <= 128 ? 128 : 256;
+  CUtensorMap tx, tw;
+  if (!make_map(&tx, X, M, K, x_half ? 2 : 1, bt, BK)) return W8A8_ERR_CUDA;
   if (wbits == 8) {
-    if (!make_map(&tb, W, N, K, BN, BK)) return W8A8_ERR_CUDA;
+    if (!make_map(&tw, W, N, K, 1, BW, BK)) return W8A8_ERR_CUDA;
   } else {
-    if (!make_map(&tb, W, N, K / 2, BN, BK / 2)) return W8A8_ERR_CUDA;
+    if (!make_map(&tw, W, N, K / 2, 1, BW, BK / 2)) return W8A8_ERR_CUDA;
   }
   unsigned int *err = device_error_word();
   if (err == nullptr) return W8A8_ERR_CUDA;
@@ -653,9 +805,9 @@ int launch_gemm_tc(const int8_t *xq, const float *sa, const void *W, const float
     p.chunk_kb = group_size / BK;
   else
     p.chunk_kb = wbits == 8 ? 1024 / BK : 16384 / BK;
-  p.mblocks = (M + BM - 1) / BM;
-  const long nblocks = (N + BN - 1) / BN;
-  const long ntiles = static_cast<long>(p.mblocks) * nblocks;
+  p.nblocks = (N + BW - 1) / BW;
+  const long tblocks = (M + bt - 1) / bt;
+  const long ntiles = static_cast<long>(p.nblocks) * tblocks;
   if (ntiles > 0x7fffffffL) return W8A8_ERR_INVALID_ARG;
   p.ntiles = static_cast<int>(ntiles);
   p.sa = sa;
@@ -663,9 +815,11 @@ int launch_gemm_tc(const int8_t *xq, const float *sa, const void *W, const float
   p.y = y;
   p.acc_out = acc_out;
   p.err = err;
-  if (wbits == 4) return launch_t<4, false>(ta, tb, p, s);
-  if (group_size != 0) return launch_t<8, true>(ta, tb, p, s);
-  return launch_t<8, false>(ta, tb, p, s);
+  if (x_half)
+    return bt == 128 ? launch_modes<true, 128>(tx, tw, p, wbits, s)
+                     : launch_modes<true, 256>(tx, tw, p, wbits, s);
+  return bt == 128 ? launch_modes<false, 128>(tx, tw, p, wbits, s)
+                   : launch_modes<false, 256>(tx, tw, p, wbits, s);
 }
 
 }  // namespace w8a8

@@ -7,13 +7,16 @@
 // 생각보다 높습니다", section "INT8 TensorOps 커널 설계", steps 3-4 (INT32
 // accumulation, rescale by s_a * s_w).
 //
-// Design (HBM-bound: the weight matrix is streamed once): each CTA stages the
-// quantized activation row in shared memory; each warp owns ROWS weight rows
-// at a time and its lanes read consecutive 16-byte chunks of each row
-// (coalesced 512-byte warp loads, non-allocating in L1), with UNROLL chunks
-// per row in flight.  Products are summed exactly with dp4a into int32 and
-// reduced across the warp with shuffles; the dequant is one fp32 scale
-// product, one multiply and one fp16 rounding, as on the GEMM path.
+// Design (HBM-bound: the weight matrix is streamed once): one warp per
+// weight row.  Lane l reads 16-byte chunks l, l + 32, ... of the row, so
+// every warp load is a coalesced 512-byte transaction, and issues up to
+// kUnroll of them before the first use (the whole row for K <= 4096) to keep
+// enough bytes in flight; weight loads bypass L1 allocation.  The quantized
+// activation row is read through the read-only cache (every warp of the
+// grid reads the same K bytes).  Products are summed exactly in int32 with
+// dp4a and reduced across the warp with shuffles; the dequant is one fp32
+// scale product, one multiply and one fp16 rounding, as on the GEMM path.
+// Few registers per thread keep many warps resident per SM.
 #include "common.cuh"
 
 namespace w8a8 {
@@ -21,7 +24,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRows = 2;
 constexpr int kUnroll = 8;
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
@@ -65,200 +67,121 @@ __global__ void __launch_bounds__(kThreads) gemv_w8a8_kernel(
     const int8_t *__restrict__ xq, const float *__restrict__ sa,
     const int8_t *__restrict__ Wq, const float *__restrict__ sw, int N, int K,
     int gs, __half *__restrict__ y) {
-  extern __shared__ uint4 xs[];
-  const int nchunk = K >> 4;
-  for (int i = threadIdx.x; i < nchunk; i += kThreads)
-    xs[i] = __ldg(reinterpret_cast<const uint4 *>(xq) + i);
-  __syncthreads();
-
   const int lane = threadIdx.x & 31;
-  const int warp = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const int nwarps = gridDim.x * kWarps;
+  const int nchunk = K >> 4;
   const int G = gs == 0 ? 1 : K / gs;
   const int cpg = gs >> 4;  // 16-byte chunks per group (4 or 8)
-
-  for (long n0 = static_cast<long>(warp) * kRows; n0 < N;
-       n0 += static_cast<long>(nwarps) * kRows) {
-    int acc[kRows];
-    float f[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) { acc[r] = 0; f[r] = 0.f; }
-    const uint4 *wrow[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      long n = n0 + r < N ? n0 + r : N - 1;  // clamp: duplicate row, not stored
-      wrow[r] = reinterpret_cast<const uint4 *>(Wq + n * K);
-    }
+  const uint4 *xv = reinterpret_cast<const uint4 *>(xq);
+  for (long n = static_cast<long>(blockIdx.x) * kWarps + (threadIdx.x >> 5); n < N;
+       n += static_cast<long>(gridDim.x) * kWarps) {
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(Wq + n * K);
+    int acc = 0;
+    float f = 0.f;
     for (int c0 = 0; c0 < nchunk; c0 += 32 * kUnroll) {
-      uint4 w[kRows][kUnroll];
+      uint4 w[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int c = c0 + u * 32 + lane;
-#pragma unroll
-        for (int r = 0; r < kRows; ++r)
-          w[r][u] = c < nchunk ? ld_stream(wrow[r] + c) : make_uint4(0, 0, 0, 0);
+        w[u] = c < nchunk ? ld_stream(wrow + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int c = c0 + u * 32 + lane;
-        const uint4 a = c < nchunk ? xs[c] : make_uint4(0, 0, 0, 0);
+        const uint4 a = c < nchunk ? __ldg(xv + c) : make_uint4(0, 0, 0, 0);
         if (gs == 0) {
-#pragma unroll
-          for (int r = 0; r < kRows; ++r) acc[r] = dot16(w[r][u], a, acc[r]);
+          acc = dot16(w[u], a, acc);
         } else {
           // the cpg lanes of one group reduce their exact partial, then the
           // group's first lane rescales it
-          const int g = (c < nchunk ? c : nchunk - 1) / cpg;
-#pragma unroll
-          for (int r = 0; r < kRows; ++r) {
-            int p = dot16(w[r][u], a, 0);
-            for (int o = cpg >> 1; o > 0; o >>= 1)
-              p += __shfl_xor_sync(0xffffffffu, p, o);
-            if ((lane & (cpg - 1)) == 0 && c < nchunk) {
-              const long n = n0 + r < N ? n0 + r : N - 1;
-              const float s = __fmul_rn(sa[g], sw[n * G + g]);
-              f[r] = __fadd_rn(f[r], __fmul_rn(static_cast<float>(p), s));
-            }
+          int p = dot16(w[u], a, 0);
+          for (int o = cpg >> 1; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+          if ((lane & (cpg - 1)) == 0 && c < nchunk) {
+            const int g = c / cpg;
+            const float s = __fmul_rn(__ldg(sa + g), __ldg(sw + n * G + g));
+            f = __fadd_rn(f, __fmul_rn(static_cast<float>(p), s));
           }
         }
       }
     }
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const long n = n0 + r;
-      if (gs == 0) {
-        const int tot = warp_sum(acc[r]);
-        if (lane == 0 && n < N)
-          y[n] = __float2half_rn(
-              __fmul_rn(static_cast<float>(tot), __fmul_rn(sa[0], sw[n])));
-      } else {
-        const float tot = warp_sumf(f[r]);
-        if (lane == 0 && n < N) y[n] = __float2half_rn(tot);
-      }
+    if (gs == 0) {
+      const int tot = warp_sum(acc);
+      if (lane == 0)
+        y[n] = __float2half_rn(
+            __fmul_rn(static_cast<float>(tot), __fmul_rn(__ldg(sa), __ldg(sw + n))));
+    } else {
+      const float tot = warp_sumf(f);
+      if (lane == 0) y[n] = __float2half_rn(tot);
     }
   }
 }
 
 // W4A8: weights packed two nibbles per byte along K (low nibble = even k).
-// Shared memory holds the activations re-ordered per block of 8 elements as
-// (a0 a2 a4 a6)(a1 a3 a5 a7), so that the even / odd nibbles of a 32-bit
-// weight word meet their activations in one dp4a each.  A nibble v in
-// [-8, 7] is read as the unsigned u = v + 8 (its top bit flipped), so
-// sum_k a_k v_k = sum_k a_k u_k - 8 sum_k a_k, all exact in int32.
+// A packed 32-bit word holds 8 consecutive k; its even nibbles meet the
+// activations (a0 a2 a4 a6) and its odd nibbles (a1 a3 a5 a7) in one dp4a
+// each.  A nibble v in [-8, 7] is read as the unsigned u = v + 8 (its top
+// bit flipped), so sum_k a_k v_k = sum_k a_k u_k - 8 sum_k a_k, all exact in
+// int32.
 __global__ void __launch_bounds__(kThreads) gemv_w4a8_kernel(
     const int8_t *__restrict__ xq, const float *__restrict__ sa,
     const uint8_t *__restrict__ Wp, const float *__restrict__ sw, int N, int K,
     __half *__restrict__ y) {
-  extern __shared__ uint4 xs[];
-  __shared__ int s_sum;
-  uint2 *xs2 = reinterpret_cast<uint2 *>(xs);
-  if (threadIdx.x == 0) s_sum = 0;
-  __syncthreads();
-  int part = 0;
-  for (int b = threadIdx.x; b < (K >> 3); b += kThreads) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(xq) + b);
-    // bytes a0..a7 -> (a0 a2 a4 a6), (a1 a3 a5 a7)
-    const uint32_t ev = __byte_perm(v.x, v.y, 0x6420);
-    const uint32_t od = __byte_perm(v.x, v.y, 0x7531);
-    xs2[b] = make_uint2(ev, od);
-    part = __dp4a(static_cast<int>(v.x), 0x01010101, part);
-    part = __dp4a(static_cast<int>(v.y), 0x01010101, part);
-  }
-  part = warp_sum(part);
-  if ((threadIdx.x & 31) == 0) atomicAdd(&s_sum, part);
-  __syncthreads();
-  const int sum_a = s_sum;
-
   const int lane = threadIdx.x & 31;
-  const int warp = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const int nwarps = gridDim.x * kWarps;
   const int nchunk = K >> 5;  // 16-byte chunks of packed weights (32 k each)
   const int rowbytes = K >> 1;
-
-  for (long n0 = static_cast<long>(warp) * kRows; n0 < N;
-       n0 += static_cast<long>(nwarps) * kRows) {
-    int acc[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) acc[r] = 0;
-    const uint4 *wrow[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      long n = n0 + r < N ? n0 + r : N - 1;
-      wrow[r] = reinterpret_cast<const uint4 *>(Wp + n * rowbytes);
-    }
+  const uint4 *xv = reinterpret_cast<const uint4 *>(xq);
+  for (long n = static_cast<long>(blockIdx.x) * kWarps + (threadIdx.x >> 5); n < N;
+       n += static_cast<long>(gridDim.x) * kWarps) {
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(Wp + n * rowbytes);
+    int acc = 0, asum = 0;
     for (int c0 = 0; c0 < nchunk; c0 += 32 * kUnroll) {
-      uint4 w[kRows][kUnroll];
+      uint4 w[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int c = c0 + u * 32 + lane;
-#pragma unroll
-        for (int r = 0; r < kRows; ++r)
-          w[r][u] = c < nchunk ? ld_stream(wrow[r] + c) : make_uint4(0, 0, 0, 0);
+        w[u] = c < nchunk ? ld_stream(wrow + c) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int c = c0 + u * 32 + lane;
         if (c >= nchunk) continue;
-        // chunk c covers k in [32c, 32c + 32): four 8-element blocks
-        const uint4 a0 = xs[2 * c], a1 = xs[2 * c + 1];
-        const uint32_t ae[4] = {a0.x, a0.z, a1.x, a1.z};
-        const uint32_t ao[4] = {a0.y, a0.w, a1.y, a1.w};
+        // chunk c covers k in [32c, 32c + 32): activations 32c .. 32c + 31
+        const uint4 a0 = __ldg(xv + 2 * c), a1 = __ldg(xv + 2 * c + 1);
+        const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          const uint32_t ww[4] = {w[r][u].x, w[r][u].y, w[r][u].z, w[r][u].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t wx = ww[j] ^ 0x88888888u;
-            acc[r] = dp4a_su(ae[j], wx & 0x0f0f0f0fu, acc[r]);
-            acc[r] = dp4a_su(ao[j], (wx >> 4) & 0x0f0f0f0fu, acc[r]);
-          }
+        for (int j = 0; j < 4; ++j) {
+          // activations of k = 8j .. 8j + 7 of the chunk: even and odd lanes
+          const uint32_t ev = __byte_perm(av[2 * j], av[2 * j + 1], 0x6420);
+          const uint32_t od = __byte_perm(av[2 * j], av[2 * j + 1], 0x7531);
+          const uint32_t wx = ww[j] ^ 0x88888888u;
+          acc = dp4a_su(ev, wx & 0x0f0f0f0fu, acc);
+          acc = dp4a_su(od, (wx >> 4) & 0x0f0f0f0fu, acc);
+          asum = __dp4a(static_cast<int>(av[2 * j]), 0x01010101, asum);
+          asum = __dp4a(static_cast<int>(av[2 * j + 1]), 0x01010101, asum);
         }
       }
     }
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const long n = n0 + r;
-      const int tot = warp_sum(acc[r]) - 8 * sum_a;
-      if (lane == 0 && n < N)
-        y[n] = __float2half_rn(
-            __fmul_rn(static_cast<float>(tot), __fmul_rn(sa[0], sw[n])));
-    }
+    const int tot = warp_sum(acc) - 8 * warp_sum(asum);
+    if (lane == 0)
+      y[n] = __float2half_rn(
+          __fmul_rn(static_cast<float>(tot), __fmul_rn(__ldg(sa), __ldg(sw + n))));
   }
 }
 
-int gemv_grid(int N) {
-  const int per_block = kWarps * kRows;
-  return (N + per_block - 1) / per_block;
-}
+int gemv_grid(int N) { return (N + kWarps - 1) / kWarps; }
 
 }  // namespace
 
 int launch_gemv_w8a8(const int8_t *xq, const float *sa, const int8_t *Wq,
                      const float *sw, int N, int K, int group_size, __half *y,
                      cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(K);
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(gemv_w8a8_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return W8A8_ERR_CUDA;
-  }
-  gemv_w8a8_kernel<<<gemv_grid(N), kThreads, smem, s>>>(xq, sa, Wq, sw, N, K,
-                                                        group_size, y);
+  gemv_w8a8_kernel<<<gemv_grid(N), kThreads, 0, s>>>(xq, sa, Wq, sw, N, K, group_size, y);
   return launch_status();
 }
 
 int launch_gemv_w4a8(const int8_t *xq, const float *sa, const uint8_t *Wp,
                      const float *sw, int N, int K, __half *y, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(K);
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(gemv_w4a8_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return W8A8_ERR_CUDA;
-  }
-  gemv_w4a8_kernel<<<gemv_grid(N), kThreads, smem, s>>>(xq, sa, Wp, sw, N, K,
-                                                        y);
+  gemv_w4a8_kernel<<<gemv_grid(N), kThreads, 0, s>>>(xq, sa, Wp, sw, N, K, y);
   return launch_status();
 }
 

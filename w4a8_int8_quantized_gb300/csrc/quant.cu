@@ -9,43 +9,58 @@
 // weights packed two per uint8 for W4A8).
 //
 // Design (HBM-bound, one streaming pass): a team of T threads (one warp for
-// K <= 4096, up to 256 threads for K <= 32768) owns one row.  Each thread loads its V 16-byte vectors (8 fp16
-// each) once into registers, the team reduces absmax with warp shuffles (and
-// shared memory when T > 32), and the same registers are quantized and stored
-// as 8-byte INT8 vectors (or one 32-bit word of 8 nibbles).  Vector i of
-// thread t covers elements [8 (i T + t), 8 (i T + t) + 8): consecutive lanes
-// read consecutive 16-byte chunks, so every warp load is one fully coalesced
-// 512-byte transaction, and a group of 64 / 128 elements is 8 / 16
-// consecutive lanes of one warp, reduced with xor shuffles inside the warp.
+// K <= 4096, up to 256 threads for K <= 32768) owns one row.  Each thread
+// loads its V 16-byte vectors (8 fp16 each) once into registers, the team
+// reduces absmax with warp shuffles (and shared memory when T > 32), and the
+// same registers are quantized and stored.  Vector i of thread t covers
+// elements [8 (i T + t), 8 (i T + t) + 8): consecutive lanes read consecutive
+// 16-byte chunks, so every warp load is one coalesced 512-byte transaction,
+// and a group of 64 / 128 elements is 8 / 16 consecutive lanes of one warp,
+// reduced with xor shuffles inside the warp.
+//
+// Outputs: INT8 codes (8-byte stores), the same codes as fp16 values (16-byte
+// stores; the operand format of the tensor-core GEMM, every code being an
+// fp16 integer exactly), or INT4 codes packed two per byte.
+//
+// Rounding: q = clamp(rint(x / s), -qmax, qmax) with x / s one IEEE fp32
+// division.  The kernel evaluates t = x * (1/s) with a correctly rounded
+// reciprocal: |t - x/s| <= |x/s| (2^-23 + 2^-48) and the IEEE quotient is
+// within |x/s| 2^-24 of x/s, so with |x/s| <= 127.01 the two differ by less
+// than 2.3e-5.  When t is farther than 2^-14 from every half-integer, both
+// lie strictly on the same side of the same half-integer and round to the
+// same integer; only the rare t within 2^-14 of a half-integer takes the
+// IEEE division itself.  The result is bit-identical to the plain rule.
 #include "common.cuh"
 
 namespace w8a8 {
 namespace {
 
+enum OutMode { kOutInt8 = 0, kOutHalf = 1, kOutInt4 = 2 };
+
 __device__ __forceinline__ float absmax8(const uint4 &v) {
   const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-  float m = 0.f;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float2 f = __half22float2(h[j]);
-    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-  }
-  return m;
+  __half2 m = __habs2(h[0]);
+  m = __hmax2(m, __habs2(h[1]));
+  m = __hmax2(m, __habs2(h[2]));
+  m = __hmax2(m, __habs2(h[3]));
+  return fmaxf(__low2float(m), __high2float(m));
 }
 
-// q = clamp(rint(x / s), -qmax, qmax); IEEE division, ties to even.
-__device__ __forceinline__ int quant1(float x, float s, float amax, int qmax) {
-  if (amax == 0.f) return 0;
-  int q = __float2int_rn(__fdiv_rn(x, s));
+// q = clamp(rint(x / s), -qmax, qmax): see the rounding note above.
+__device__ __forceinline__ int quant1(float x, float s, float rcp, int qmax) {
+  const float t = __fmul_rn(x, rcp);
+  float r = rintf(t);
+  const float to_half = 0.5f - fabsf(t - r);  // distance to the nearest half-integer
+  if (to_half <= 6.103515625e-05f) r = rintf(__fdiv_rn(x, s));
+  const int q = static_cast<int>(r);
   return max(-qmax, min(qmax, q));
 }
 
-template <int V>
+template <int V, int MODE>
 __global__ void __launch_bounds__(256) row_quant_kernel(
     const uint4 *__restrict__ x, long R, int K, int gs, int qmax, int T,
-    int8_t *__restrict__ q, uint32_t *__restrict__ packed,
-    float *__restrict__ scale) {
-  __shared__ float red[32];
+    void *__restrict__ out, float *__restrict__ scale) {
+  __shared__ float red[8];
   const int nvec = K >> 3;
   const int t = threadIdx.x % T;
   const int team = threadIdx.x / T;
@@ -95,52 +110,83 @@ __global__ void __launch_bounds__(256) row_quant_kernel(
 
   const float fq = static_cast<float>(qmax);
   const float s_row = __fdiv_rn(amax_row, fq);
+  const float rcp_row = amax_row == 0.f ? 0.f : __frcp_rn(s_row);
   if (gs == 0 && t == 0) scale[r] = s_row;
 
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int vi = i * T + t;
     if (vi >= nvec) continue;
-    float amax = amax_row, s = s_row;
+    float s = s_row, rcp = rcp_row;
     if (gs != 0) {
-      amax = vmax[i];
-      s = __fdiv_rn(amax, fq);
+      s = __fdiv_rn(vmax[i], fq);
+      rcp = vmax[i] == 0.f ? 0.f : __frcp_rn(s);
       const int g = (vi << 3) / gs;
       if ((t & ((gs >> 3) - 1)) == 0) scale[r * G + g] = s;
     }
+    // a zero row or group has s = 0 and rcp = 0: t = 0 and every code is 0
     const __half2 *h = reinterpret_cast<const __half2 *>(&v[i]);
     int qi[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float2 f = __half22float2(h[j]);
-      qi[2 * j] = quant1(f.x, s, amax, qmax);
-      qi[2 * j + 1] = quant1(f.y, s, amax, qmax);
+      qi[2 * j] = quant1(f.x, s, rcp, qmax);
+      qi[2 * j + 1] = quant1(f.y, s, rcp, qmax);
     }
-    if (packed == nullptr) {
+    if (MODE == kOutInt8) {
       uint32_t lo = (qi[0] & 0xff) | ((qi[1] & 0xff) << 8) |
                     ((qi[2] & 0xff) << 16) | ((uint32_t)(qi[3] & 0xff) << 24);
       uint32_t hi = (qi[4] & 0xff) | ((qi[5] & 0xff) << 8) |
                     ((qi[6] & 0xff) << 16) | ((uint32_t)(qi[7] & 0xff) << 24);
-      reinterpret_cast<uint2 *>(q + r * K)[vi] = make_uint2(lo, hi);
+      reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + r * K)[vi] = make_uint2(lo, hi);
+    } else if (MODE == kOutHalf) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        __half2 hh = __halves2half2(__int2half_rn(qi[2 * j]), __int2half_rn(qi[2 * j + 1]));
+        w[j] = *reinterpret_cast<uint32_t *>(&hh);
+      }
+      reinterpret_cast<uint4 *>(static_cast<__half *>(out) + r * K)[vi] =
+          make_uint4(w[0], w[1], w[2], w[3]);
     } else {
       uint32_t w = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) w |= (uint32_t)(qi[j] & 0xf) << (4 * j);
-      packed[r * (K >> 3) + vi] = w;
+      static_cast<uint32_t *>(out)[r * (K >> 3) + vi] = w;
     }
   }
 }
 
-template <int V>
-int launch_v(const __half *x, long R, int K, int gs, int qmax, int T,
-             int8_t *q, uint8_t *packed, float *scale, cudaStream_t s) {
+template <int V, int MODE>
+int launch_v(const __half *x, long R, int K, int gs, int qmax, int T, void *out,
+             float *scale, cudaStream_t s) {
   const int block = 256;
   const int rows_per_block = block / T;
   const long grid = (R + rows_per_block - 1) / rows_per_block;
-  row_quant_kernel<V><<<static_cast<unsigned>(grid), block, 0, s>>>(
-      reinterpret_cast<const uint4 *>(x), R, K, gs, qmax, T, q,
-      reinterpret_cast<uint32_t *>(packed), scale);
+  row_quant_kernel<V, MODE><<<static_cast<unsigned>(grid), block, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), R, K, gs, qmax, T, out, scale);
   return launch_status();
+}
+
+template <int MODE>
+int launch_mode(const __half *x, int R, int K, int group_size, int qmax, void *out,
+                float *scale, cudaStream_t s) {
+  const int nvec = K >> 3;
+  int T = 32;
+  while (T < 256 && (nvec + T - 1) / T > 16) T <<= 1;
+  const int V = (nvec + T - 1) / T;
+  switch (V) {
+#define W8A8_CASE(n) \
+  case n:            \
+    return launch_v<n, MODE>(x, R, K, group_size, qmax, T, out, scale, s);
+    W8A8_CASE(1) W8A8_CASE(2) W8A8_CASE(3) W8A8_CASE(4) W8A8_CASE(5)
+    W8A8_CASE(6) W8A8_CASE(7) W8A8_CASE(8) W8A8_CASE(9) W8A8_CASE(10)
+    W8A8_CASE(11) W8A8_CASE(12) W8A8_CASE(13) W8A8_CASE(14) W8A8_CASE(15)
+    W8A8_CASE(16)
+#undef W8A8_CASE
+    default:
+      return W8A8_ERR_INVALID_ARG;  // K > 32768
+  }
 }
 
 }  // namespace
@@ -148,23 +194,15 @@ int launch_v(const __half *x, long R, int K, int gs, int qmax, int T,
 int launch_row_quant(const __half *x, int R, int K, int group_size, int qmax,
                      int8_t *q, uint8_t *packed, float *scale, cudaStream_t s) {
   if (R == 0) return W8A8_OK;
-  const int nvec = K >> 3;
-  int T = 32;
-  while (T < 256 && (nvec + T - 1) / T > 16) T <<= 1;
-  const int V = (nvec + T - 1) / T;
-  if (V > 16) return W8A8_ERR_INVALID_ARG;  // K > 32768
-  switch (V) {
-#define W8A8_CASE(n) \
-  case n:            \
-    return launch_v<n>(x, R, K, group_size, qmax, T, q, packed, scale, s);
-    W8A8_CASE(1) W8A8_CASE(2) W8A8_CASE(3) W8A8_CASE(4) W8A8_CASE(5)
-    W8A8_CASE(6) W8A8_CASE(7) W8A8_CASE(8) W8A8_CASE(9) W8A8_CASE(10)
-    W8A8_CASE(11) W8A8_CASE(12) W8A8_CASE(13) W8A8_CASE(14) W8A8_CASE(15)
-    W8A8_CASE(16)
-#undef W8A8_CASE
-    default:
-      return W8A8_ERR_INVALID_ARG;
-  }
+  if (packed != nullptr)
+    return launch_mode<kOutInt4>(x, R, K, group_size, qmax, packed, scale, s);
+  return launch_mode<kOutInt8>(x, R, K, group_size, qmax, q, scale, s);
+}
+
+int launch_row_quant_half(const __half *x, int R, int K, int group_size, __half *qh,
+                          float *scale, cudaStream_t s) {
+  if (R == 0) return W8A8_OK;
+  return launch_mode<kOutHalf>(x, R, K, group_size, 127, qh, scale, s);
 }
 
 }  // namespace w8a8
