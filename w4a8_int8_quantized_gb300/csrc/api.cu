@@ -94,6 +94,14 @@ int gemm_dispatch(const int8_t *xq, const float *sa, const void *W,
   return launch_gemm_tc(xq, false, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
 }
 
+// fp16 activation codes: CTA-pair GEMM for M > 128 (256-token pair tiles),
+// single-CTA GEMM with 128-token tiles otherwise
+int gemm_h_dispatch(const void *xq_h, const float *sa, const void *W, const float *sw,
+                    int M, int N, int K, int gs, int wbits, __half *y, cudaStream_t s) {
+  if (M > 128) return launch_gemm_tc_pair(xq_h, sa, W, sw, M, N, K, gs, wbits, y, s);
+  return launch_gemm_tc(xq_h, true, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
+}
+
 }  // namespace
 }  // namespace w8a8
 
@@ -214,8 +222,8 @@ int w8a8_gemm_h(const w8a8_half *xq_h, const float *scale_a, const void *Wq,
   W8A8_TRY(check_ptrs16({xq_h, Wq, y}));
   W8A8_TRY(check_ptrs4({scale_a, scale_w}));
   W8A8_TRY(check_device());
-  return launch_gemm_tc(xq_h, true, scale_a, Wq, scale_w, M, N, K, group_size, wbits,
-                        reinterpret_cast<__half *>(y), nullptr, as_stream(stream));
+  return gemm_h_dispatch(xq_h, scale_a, Wq, scale_w, M, N, K, group_size, wbits,
+                         reinterpret_cast<__half *>(y), as_stream(stream));
 }
 
 size_t w8a8_linear_workspace_bytes(int M, int K, int group_size) {
@@ -253,8 +261,8 @@ int linear(const w8a8_half *x, const void *Wq, const float *scale_w, int M,
   __half *xq_h = static_cast<__half *>(workspace);
   W8A8_TRY(launch_row_quant_half(reinterpret_cast<const __half *>(x), M, K, group_size, xq_h,
                                  sa, s));
-  return launch_gemm_tc(xq_h, true, sa, Wq, scale_w, M, N, K, group_size, wbits,
-                        reinterpret_cast<__half *>(y), nullptr, s);
+  return gemm_h_dispatch(xq_h, sa, Wq, scale_w, M, N, K, group_size, wbits,
+                         reinterpret_cast<__half *>(y), s);
 }
 
 int w8a8_gemm_i32(const int8_t *xq, const void *Wq, int M, int N, int K,

@@ -7,7 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/w8a8.h"
+#include "w8a8.h"  // include/, on the include path
 
 namespace w8a8 {
 
@@ -80,5 +80,10 @@ int launch_row_quant_half(const __half *x, int R, int K, int group_size, __half 
 int launch_gemm_tc(const void *A, bool a_half, const float *sa, const void *W,
                    const float *sw, int M, int N, int K, int group_size, int wbits,
                    __half *y, int32_t *acc_out, cudaStream_t s);
+
+// The same GEMM on CTA pairs (cta_group::2) for fp16 activation codes; used
+// for M > 128.
+int launch_gemm_tc_pair(const void *X, const float *sa, const void *W, const float *sw, int M,
+                        int N, int K, int group_size, int wbits, __half *y, cudaStream_t s);
 
 }  // namespace w8a8
