@@ -94,11 +94,9 @@ int gemm_dispatch(const int8_t *xq, const float *sa, const void *W,
   return launch_gemm_tc(xq, false, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
 }
 
-// fp16 activation codes: CTA-pair GEMM for M > 128 (256-token pair tiles),
-// single-CTA GEMM with 128-token tiles otherwise
+// fp16 activation codes: the tensor-core GEMM for any M
 int gemm_h_dispatch(const void *xq_h, const float *sa, const void *W, const float *sw,
                     int M, int N, int K, int gs, int wbits, __half *y, cudaStream_t s) {
-  if (M > 128) return launch_gemm_tc_pair(xq_h, sa, W, sw, M, N, K, gs, wbits, y, s);
   return launch_gemm_tc(xq_h, true, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
 }
 

@@ -81,9 +81,4 @@ int launch_gemm_tc(const void *A, bool a_half, const float *sa, const void *W,
                    const float *sw, int M, int N, int K, int group_size, int wbits,
                    __half *y, int32_t *acc_out, cudaStream_t s);
 
-// The same GEMM on CTA pairs (cta_group::2) for fp16 activation codes; used
-// for M > 128.
-int launch_gemm_tc_pair(const void *X, const float *sa, const void *W, const float *sw, int M,
-                        int N, int K, int group_size, int wbits, __half *y, cudaStream_t s);
-
 }  // namespace w8a8

@@ -57,36 +57,45 @@ constexpr int NUM_THREADS = 512;
 constexpr int EPI_WARPS = 8, EPI_THREADS = EPI_WARPS * 32;
 constexpr long long kTimeoutCycles = 4000000000LL;  // about 2 s at 2 GHz
 
-// Shared-memory plan.  XH: activations arrive as fp16 codes (a TMA-filled
-// ring straight into the operand layout); BT: tokens per tile.  Three
-// rings: the INT8 / INT4 staging ring (TMA -> converters), the fp16 weight
-// operand ring (converters -> MMA) and the fp16 activation operand ring
-// (TMA or converters -> MMA), each with its own depth.
+// Shared-memory plan.  XH: activations arrive as fp16 codes (TMA straight
+// into the operand layout); BT: tokens per tile (activations as INT8 codes
+// use BT = 128).  Two rings: the INT8 / INT4 staging ring (TMA ->
+// converters) and the operand stages, each holding one K block of fp16
+// weights (written by the converters) and fp16 activations (written by TMA,
+// or by the converters).  Operand stages are released REL at a time (one
+// MMA commit per REL K blocks).
 template <bool XH, int BT>
 struct Plan {
   static constexpr int W8_BYTES = BW * BK;         // INT8 weight stage (INT4 uses half)
   static constexpr int X8_BYTES = XH ? 0 : BT * BK;
-  static constexpr int W16_BYTES = BW * BK * 2;    // fp16 operand stages, 128-byte rows
+  static constexpr int W16_BYTES = BW * BK * 2;    // fp16 operands, 128-byte rows
   static constexpr int X16_BYTES = BT * BK * 2;
-  static constexpr int S8 = 3, SW = 2, SX = XH ? 5 : 3;
-  // warp roles: 0 staging producer, 1 MMA, 2 activation producer (XH) or
-  // converter, the rest up to 7 converters, 8-15 epilogue
-  static constexpr int CONV_WARPS = XH ? 5 : 6;
-  static constexpr int CONV_WARP0 = XH ? 3 : 2;
+  static constexpr int STAGE_BYTES = W16_BYTES + X16_BYTES;
+  static constexpr int S8 = 3, S = 4;               // S: operand stages
+#ifndef W8A8_TC_RELEASE
+  static constexpr int REL = 1;                    // stages released per commit
+#else
+  static constexpr int REL = W8A8_TC_RELEASE;
+#endif
+  // warp roles: 0 producers (lane 0 staging, lane 1 fp16 activations), 1
+  // MMA, 2-7 converters, 8-15 epilogue
+  static constexpr int CONV_WARPS = 6;
+  static constexpr int CONV_WARP0 = 2;
   static constexpr int CONV_THREADS = CONV_WARPS * 32;
   static constexpr int OFF_W8 = 0;
   static constexpr int OFF_X8 = OFF_W8 + S8 * W8_BYTES;
-  static constexpr int OFF_W16 = OFF_X8 + S8 * X8_BYTES;
-  static constexpr int OFF_X16 = OFF_W16 + SW * W16_BYTES;
-  static constexpr int OFF_SA = OFF_X16 + SX * X16_BYTES;   // 2 x BT fp32 scales
+  static constexpr int OFF_ST = OFF_X8 + S8 * X8_BYTES;    // stage s: W16, then X16
+  static constexpr int OFF_SA = OFF_ST + S * STAGE_BYTES;  // 2 x BT fp32 scales
   static constexpr int OFF_BAR = OFF_SA + 2 * BT * 4;
-  static constexpr int NUM_BARS = 2 * S8 + 2 * SW + 2 * SX + 2 + 2 + 2 + 1;
+  static constexpr int NUM_BARS = 2 * S8 + S + S / REL + 2 + 2 + 2 + 1;
   static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + align slack
   static constexpr uint32_t TMEM_COLS = 2 * BT;  // two accumulators of BT fp32 columns
-  static_assert(OFF_W16 % 1024 == 0 && OFF_X16 % 1024 == 0, "swizzled stages need 1 KB alignment");
+  static_assert(OFF_ST % 1024 == 0 && W16_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0,
+                "swizzled stages need 1 KB alignment");
+  static_assert(S % REL == 0, "stages are released in groups of REL");
 };
 static_assert(Plan<true, 256>::SMEM_BYTES <= 232448, "shared memory plan too large");
-static_assert(Plan<false, 256>::SMEM_BYTES <= 232448, "shared memory plan too large");
+static_assert(Plan<false, 128>::SMEM_BYTES <= 232448, "shared memory plan too large");
 
 // instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
 // M = 128 (weights), N = BT (tokens)
@@ -125,31 +134,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// arrive on a barrier named by a shared::cluster address (own or peer CTA)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
-}
-
-// shared::cluster address of `local` in CTA `rank` of this cluster
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -267,33 +251,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
   }
 }
 
-// Bounded wait with cluster-scope acquire (barriers that a peer CTA or a
-// multicast commit arrives on).
-__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity,
-                                                 volatile int *abort_flag, unsigned int code,
-                                                 unsigned int *err) {
-#pragma unroll 1
-  for (int i = 0; i < 32; ++i)
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
-      if (err != nullptr) atomicCAS(err, 0u, code);
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
-template <bool CLUSTER>
-__device__ __forceinline__ bool wait_any(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         unsigned int code, unsigned int *err) {
-  return CLUSTER ? wait_bar_cluster(bar, parity, abort_flag, code, err)
-                 : wait_bar(bar, parity, abort_flag, code, err);
-}
-
 // Bounded wait that ignores the abort flag (teardown: let own work land).
 __device__ __forceinline__ void wait_bar_teardown(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
@@ -346,35 +303,51 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int j) {
 }
 
 // Converts `rows` rows x 64 codes of a staged tile into the swizzled fp16
-// operand tile; unit u = (row u / 8, 8-element group u % 8).  Four units per
-// thread are loaded before any is converted, for memory-level parallelism.
+// operand tile.  Unit u = (row u / 4, codes 16 (u % 4) .. +16): one 16-byte
+// load (8 bytes of packed INT4) and two 16-byte stores into swizzled chunks
+// 2 (u % 4) and 2 (u % 4) + 1.  A warp covers 8 whole rows; each 8-thread
+// store phase writes two rows' even (or odd) chunks, which the 128-byte
+// swizzle puts in disjoint banks.  Two units per thread are loaded before
+// either is converted.
 template <bool INT4, int NT>
 __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, int rows,
                                              int ct) {
-  const int units = rows * 8;
+  const int units = rows * 4;
 #pragma unroll 1
-  for (int u0 = ct; u0 < units; u0 += 4 * NT) {
-    uint2 v[4];
+  for (int u0 = ct; u0 < units; u0 += 2 * NT) {
+    uint4 v[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       const int u = u0 + i * NT;
-      v[i] = make_uint2(0, 0);
+      v[i] = make_uint4(0, 0, 0, 0);
       if (u < units) {
-        const int r = u >> 3, j = u & 7;
+        const int r = u >> 2, c = u & 3;
         if (INT4) {
-          v[i].x = *reinterpret_cast<const uint32_t *>(src + r * 32 + j * 4);
+          const uint2 w = *reinterpret_cast<const uint2 *>(src + r * 32 + c * 8);
+          v[i].x = w.x;
+          v[i].y = w.y;
         } else {
-          v[i] = *reinterpret_cast<const uint2 *>(src + r * 64 + j * 8);
+          v[i] = *reinterpret_cast<const uint4 *>(src + r * 64 + c * 16);
         }
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       const int u = u0 + i * NT;
       if (u < units) {
-        const int r = u >> 3, j = u & 7;
-        const uint4 o = INT4 ? i4x8_to_h(v[i].x) : i8x8_to_h(v[i]);
-        *reinterpret_cast<uint4 *>(dst + sw128_off(r, j)) = o;
+        const int r = u >> 2, c = u & 3;
+        uint4 lo, hi;
+        if (INT4) {
+          lo = i4x8_to_h(v[i].x);
+          hi = i4x8_to_h(v[i].y);
+        } else {
+          lo = i8x8_to_h(make_uint2(v[i].x, v[i].y));
+          hi = i8x8_to_h(make_uint2(v[i].z, v[i].w));
+        }
+        uint8_t *row = dst + (r >> 3) * 1024 + (r & 7) * 128;
+        const int x = r & 7;
+        *reinterpret_cast<uint4 *>(row + (((2 * c) ^ x) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ x) << 4)) = hi;
       }
     }
   }
@@ -387,19 +360,14 @@ __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, i
 // lane quadrant q and tokens [h BT/2, (h+1) BT/2).  Tiles are
 // tile0, tile0 + tile_step, ...; tile t covers channels
 // (t % nblocks) * ch_block + ch_off + [0, 128) and tokens (t / nblocks) * BT
-// + [0, BT).  Each warp arrives on the local barrier accempty0 (+8 per
-// accumulator) when its share of a chunk is drained.  With forward_remote0
-// set (the non-leader CTA of a pair), lane 0 of warp 8 then waits for all 8
-// warps and forwards one cluster-scope arrive to that shared::cluster
-// address (the leader's accumulator-free barrier).  CLUSTER selects
-// cluster-scope waits.
-template <bool PERGROUP, int BT, bool CLUSTER>
+// + [0, BT).  Each warp arrives on accempty0 (+8 per accumulator) when its
+// share of a chunk is drained.
+template <bool PERGROUP, int BT>
 __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, uint32_t base,
                                               uint8_t *sm, int off_sa, int warp, int lane,
                                               int tile0, int tile_step, int nblocks, int ch_block,
                                               int ch_off, uint32_t accfull0, uint32_t accempty0,
-                                              uint32_t saready0, volatile int *abort_flag,
-                                              uint32_t forward_remote0 = 0) {
+                                              uint32_t saready0, volatile int *abort_flag) {
   constexpr int CPT = BT / 2;  // token columns per epilogue thread
   const int nkb = p.nkb, chunk_kb = p.chunk_kb;
   auto accfull = [&](uint32_t r) { return accfull0 + 8u * r; };
@@ -454,8 +422,7 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
           mbar_arrive(saready(gb));
           if (n < p.N) sw_g = __ldg(p.sw + n * p.G + c);
         }
-        bool w = wait_any<CLUSTER>(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier,
-                                   p.err);
+        bool w = wait_bar(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err);
         if (PERGROUP && want_y)
           w = w && wait_bar(saready(gb), gph, abort_flag, kDevErrAccumBarrier, p.err);
         if (!__all_sync(0xffffffffu, w)) {
@@ -510,15 +477,7 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(accempty(r));
-          if (forward_remote0 != 0 && warp == 8) {
-            // one cluster-scope arrive for the whole CTA (release fences are costly)
-            if (wait_bar(accempty(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err))
-              mbar_arrive_cluster(forward_remote0 + 8u * r);
-          }
-        }
-        __syncwarp();
+        if (lane == 0) mbar_arrive(accempty(r));
         ++cc;
       }
       if (!ok) break;
@@ -580,7 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmW, const TcParams p) {
   using PL = Plan<XH, BT>;
-  constexpr int S8 = PL::S8, SW = PL::SW, SX = PL::SX;
+  constexpr int S8 = PL::S8, S = PL::S;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -590,31 +549,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t bar0 = base + PL::OFF_BAR;
   auto full8 = [&](int s) { return bar0 + 8u * s; };
   auto empty8 = [&](int s) { return bar0 + 8u * (S8 + s); };
-  auto fullw = [&](int s) { return bar0 + 8u * (2 * S8 + s); };
-  auto emptyw = [&](int s) { return bar0 + 8u * (2 * S8 + SW + s); };
-  auto fullx = [&](int s) { return bar0 + 8u * (2 * S8 + 2 * SW + s); };
-  auto emptyx = [&](int s) { return bar0 + 8u * (2 * S8 + 2 * SW + SX + s); };
-  constexpr int B_ACC = 2 * S8 + 2 * SW + 2 * SX;
+  auto full = [&](int s) { return bar0 + 8u * (2 * S8 + s); };
+  constexpr int REL = PL::REL;
+  auto empty = [&](int g) { return bar0 + 8u * (2 * S8 + S + g); };  // per release group
+  constexpr int B_ACC = 2 * S8 + S + S / REL;
   auto accfull = [&](int r) { return bar0 + 8u * (B_ACC + r); };
   auto accempty = [&](int r) { return bar0 + 8u * (B_ACC + 2 + r); };
   auto saready = [&](int b) { return bar0 + 8u * (B_ACC + 4 + b); };
   const uint32_t drain_bar = bar0 + 8u * (B_ACC + 6);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + PL::OFF_BAR + PL::NUM_BARS * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  auto w16 = [&](int s) { return base + PL::OFF_ST + s * PL::STAGE_BYTES; };
+  auto x16 = [&](int s) { return base + PL::OFF_ST + s * PL::STAGE_BYTES + PL::W16_BYTES; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S8; ++s) {
       mbar_init(full8(s), 1);
       mbar_init(empty8(s), PL::CONV_WARPS);
     }
-    for (int s = 0; s < SW; ++s) {
-      mbar_init(fullw(s), PL::CONV_WARPS);
-      mbar_init(emptyw(s), 1);
-    }
-    for (int s = 0; s < SX; ++s) {
-      mbar_init(fullx(s), XH ? 1 : PL::CONV_WARPS);
-      mbar_init(emptyx(s), 1);
-    }
+    for (int s = 0; s < S; ++s) mbar_init(full(s), PL::CONV_WARPS + (XH ? 1 : 0));
+    for (int g = 0; g < S / REL; ++g) mbar_init(empty(g), 1);
     for (int r = 0; r < 2; ++r) {
       mbar_init(accfull(r), 1);
       mbar_init(accempty(r), EPI_WARPS);
@@ -648,7 +602,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // allocates registers to that limit.
   if (warp >= 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
-    epilogue_role<PERGROUP, BT, false>(p, tmem, base, sm, PL::OFF_SA, warp, lane, blockIdx.x,
+    epilogue_role<PERGROUP, BT>(p, tmem, base, sm, PL::OFF_SA, warp, lane, blockIdx.x,
                                        gridDim.x, p.nblocks, BW, 0, accfull(0), accempty(0),
                                        saready(0), abort_flag);
     tc_fence_before();
@@ -685,40 +639,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // every copy this thread issued has landed before the CTA can exit
         for (int i = 0; i < S8; ++i)
           if ((pend >> i) & 1u) wait_bar_teardown(full8(i), (pph >> i) & 1u);
-      }
-    } else if (XH && warp == 2) {
-      // ------------------------------- activation (fp16 codes) producer --
-      if (lane == 0) {
-        int sx = 0;
-        uint32_t phx = 0;
-        uint32_t pend = 0, pph = 0;
+      } else if (XH && lane == 1) {
+        // ----------------------------- activation (fp16 codes) producer --
+        int s = 0;
+        uint32_t ph = 0, pend = 0, pph = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
           const int tb = tile / p.nblocks;
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bar(emptyx(sx), phx ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
+            // a release group is refilled once the MMAs of its last use are done
+            if ((s % REL) == 0 &&
+                !wait_bar(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(fullx(sx), PL::X16_BYTES);
-            tma_load_2d(base + PL::OFF_X16 + sx * PL::X16_BYTES, &tmX, fullx(sx), kb * BK,
-                        tb * BT);
-            pend |= 1u << sx;
-            pph = (pph & ~(1u << sx)) | (phx << sx);
-            if (++sx == SX) {
-              sx = 0;
-              phx ^= 1u;
+            mbar_arrive_expect_tx(full(s), PL::X16_BYTES);
+            tma_load_2d(x16(s), &tmX, full(s), kb * BK, tb * BT);
+            pend |= 1u << s;
+            pph = (pph & ~(1u << s)) | (ph << s);
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
             }
           }
         }
-        for (int i = 0; i < SX; ++i)
-          if ((pend >> i) & 1u) wait_bar_teardown(fullx(i), (pph >> i) & 1u);
+        for (int i = 0; i < S; ++i)
+          if ((pend >> i) & 1u) wait_bar_teardown(full(i), (pph >> i) & 1u);
       }
     } else if (warp == 1) {
       // ---------------------------------------------------- MMA issuer ----
       if (lane == 0) {
-        int sw = 0, sx = 0;
-        uint32_t phw = 0, phx = 0, cc = 0;
+        int s = 0;
+        uint32_t ph = 0, cc = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
           for (int kb = 0; kb < nkb; ++kb) {
@@ -732,37 +684,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               tc_fence_after();
             }
-            if (!wait_bar(fullx(sx), phx, abort_flag, kDevErrFullBarrier, p.err) ||
-                !wait_bar(fullw(sw), phw, abort_flag, kDevErrFullBarrier, p.err)) {
+            if (!wait_bar(full(s), ph, abort_flag, kDevErrFullBarrier, p.err)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t d = tmem + r * BT;
-            const uint32_t w_base = base + PL::OFF_W16 + sw * PL::W16_BYTES;
-            const uint32_t x_base = base + PL::OFF_X16 + sx * PL::X16_BYTES;
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              tc_mma(d, sw128_desc(w_base + k * 32), sw128_desc(x_base + k * 32), idesc<BT>(),
+              tc_mma(d, sw128_desc(w16(s) + k * 32), sw128_desc(x16(s) + k * 32), idesc<BT>(),
                      (first && k == 0) ? 0u : 1u);
             }
-            tc_commit(emptyw(sw));
-            tc_commit(emptyx(sx));
+            if ((s % REL) == REL - 1) tc_commit(empty(s / REL));
             if ((kb % chunk_kb) == chunk_kb - 1 || kb == nkb - 1) {
               tc_commit(accfull(r));
               ++cc;
             }
-            if (++sw == SW) {
-              sw = 0;
-              phw ^= 1u;
-            }
-            if (++sx == SX) {
-              sx = 0;
-              phx ^= 1u;
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
             }
           }
         }
-        // all MMAs issued here have completed before TMEM is freed
+        // release a partly used last group, then let every MMA land before TMEM is freed
+        if ((s % REL) != 0) tc_commit(empty(s / REL));
         tc_commit(drain_bar);
         wait_bar_teardown(drain_bar, 0);
       }
@@ -770,41 +715,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---------------------------------------------------- converters ----
       constexpr int NT = PL::CONV_THREADS;
       const int ct = (warp - PL::CONV_WARP0) * 32 + lane;
-      int s8 = 0, sw = 0, sx = 0;
-      uint32_t ph8 = 0, phw = 0, phx = 0;
+      int s8 = 0, s = 0;
+      uint32_t ph8 = 0, ph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb) {
           bool w = wait_bar(full8(s8), ph8, abort_flag, kDevErrFullBarrier, p.err);
-          w = w && wait_bar(emptyw(sw), phw ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err);
-          if (!XH) w = w && wait_bar(emptyx(sx), phx ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err);
+          if ((s % REL) == 0)
+            w = w && wait_bar(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err);
           if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
           }
           convert_tile<WBITS == 4, NT>(sm + PL::OFF_W8 + s8 * PL::W8_BYTES,
-                                       sm + PL::OFF_W16 + sw * PL::W16_BYTES, BW, ct);
+                                       sm + (w16(s) - base), BW, ct);
           if (!XH)
-            convert_tile<false, NT>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES,
-                                    sm + PL::OFF_X16 + sx * PL::X16_BYTES, BT, ct);
+            convert_tile<false, NT>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES, sm + (x16(s) - base),
+                                    BT, ct);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(fullw(sw));
-            if (!XH) mbar_arrive(fullx(sx));
+            mbar_arrive(full(s));
             mbar_arrive(empty8(s8));
           }
           if (++s8 == S8) {
             s8 = 0;
             ph8 ^= 1u;
           }
-          if (++sw == SW) {
-            sw = 0;
-            phw ^= 1u;
-          }
-          if (!XH && ++sx == SX) {
-            sx = 0;
-            phx ^= 1u;
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
           }
         }
       }
@@ -818,339 +758,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(PL::TMEM_COLS));
-  }
-}
-
-// ------------------------------------------------------ 2-CTA kernel ----
-//
-// The same contraction on CTA pairs (a cluster of 2, tcgen05 cta_group::2):
-// one M = 256 x N = 256 x K = 16 MMA spans both SMs.  CTA r of the pair
-// holds its own 128 output channels of the weights (A) and 128 of the 256
-// tokens of the activations (B) in its shared memory; the MMA reads both
-// CTAs' halves and writes each CTA's 128 channels x 256 tokens into that
-// CTA's TMEM.  Per SM this halves the activation bytes per K block (16 KB),
-// so six K blocks fit in shared memory.  The leader CTA (rank 0) issues the
-// MMAs; its stage-full barriers count the converter warps of both CTAs (each
-// converter warp has also seen its own CTA's activation copy land), its
-// accumulator-free barriers count the epilogue warps of both CTAs, and its
-// commits are multicast to the barriers of both CTAs.  Stages are released
-// two K blocks at a time: a release commit every K block costs a measurable
-// share of the tensor pipe, one every two does not.
-// Activations arrive as fp16 codes only (the path linear() uses for M > 1).
-
-constexpr int P_BT = 256;                  // tokens per pair tile (128 per CTA)
-constexpr int P_S8 = 3, P_S = 6;           // staging ring, operand stages (pairs of 2)
-constexpr int P_CONV_WARPS = 5, P_CONV_WARP0 = 3;
-constexpr int P_W8_BYTES = BW * BK;        // this CTA's 128 channels
-constexpr int P_W16_BYTES = BW * BK * 2;
-constexpr int P_X16_BYTES = (P_BT / 2) * BK * 2;
-constexpr int P_OFF_W8 = 0;
-constexpr int P_OFF_W16 = P_OFF_W8 + P_S8 * P_W8_BYTES;
-constexpr int P_OFF_X16 = P_OFF_W16 + P_S * P_W16_BYTES;
-constexpr int P_OFF_SA = P_OFF_X16 + P_S * P_X16_BYTES;
-constexpr int P_OFF_BAR = P_OFF_SA + 2 * P_BT * 4;
-// full8, empty8 [S8]; xfull, full [S]; empty [S/2]; accfull, accempty, saready [2]; drain;
-// wfull [S]; accfree [2]
-constexpr int P_NUM_BARS = 2 * P_S8 + 2 * P_S + P_S / 2 + 2 + 2 + 2 + 1 + P_S + 2;
-constexpr int P_SMEM_BYTES = P_OFF_BAR + P_NUM_BARS * 8 + 16 + 1024;
-static_assert(P_OFF_W16 % 1024 == 0 && P_OFF_X16 % 1024 == 0, "swizzled stages need 1 KB alignment");
-static_assert(P_SMEM_BYTES <= 232448, "shared memory plan too large");
-static_assert(P_S % 2 == 0, "stages are released in pairs");
-
-// kind::f16 instruction descriptor for the pair MMA: M = 256, N = 256
-constexpr uint32_t P_IDESC = (1u << 4) | (static_cast<uint32_t>(P_BT >> 3) << 17) |
-                             (static_cast<uint32_t>(256 >> 4) << 24);
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-__device__ __forceinline__ void tc2_mma(uint32_t d, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t accum) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(P_IDESC), "r"(accum));
-}
-
-// arrive on the barrier at this offset in both CTAs of the pair once all
-// MMAs issued so far have completed
-__device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(static_cast<uint16_t>(3))
-      : "memory");
-}
-
-template <int WBITS, bool PERGROUP>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmX,
-                    const __grid_constant__ CUtensorMap tmW, const TcParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t *sm = smem_raw + (base - raw);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
-  const int pair0 = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int nblocks2 = p.nblocks;  // 256-channel blocks
-
-  const uint32_t bar0 = base + P_OFF_BAR;
-  auto full8 = [&](int s) { return bar0 + 8u * s; };
-  auto empty8 = [&](int s) { return bar0 + 8u * (P_S8 + s); };
-  auto xfull = [&](int s) { return bar0 + 8u * (2 * P_S8 + s); };
-  auto full = [&](int s) { return bar0 + 8u * (2 * P_S8 + P_S + s); };
-  auto empty = [&](int pr) { return bar0 + 8u * (2 * P_S8 + 2 * P_S + pr); };
-  constexpr int B_ACC = 2 * P_S8 + 2 * P_S + P_S / 2;
-  auto accfull = [&](int r) { return bar0 + 8u * (B_ACC + r); };
-  auto accempty = [&](int r) { return bar0 + 8u * (B_ACC + 2 + r); };
-  auto saready = [&](int b) { return bar0 + 8u * (B_ACC + 4 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (B_ACC + 6);
-  auto wfull = [&](int s) { return bar0 + 8u * (B_ACC + 7 + s); };
-  auto accfree = [&](int r) { return bar0 + 8u * (B_ACC + 7 + P_S + r); };
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + P_OFF_BAR + P_NUM_BARS * 8);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < P_S8; ++s) {
-      mbar_init(full8(s), 1);
-      mbar_init(empty8(s), P_CONV_WARPS);
-    }
-    for (int s = 0; s < P_S; ++s) {
-      mbar_init(xfull(s), 1);
-      // leader: its own converter warps + one forwarded arrive from the peer
-      mbar_init(full(s), P_CONV_WARPS + 1);
-      mbar_init(wfull(s), P_CONV_WARPS);  // peer: its converter warps
-    }
-    for (int pr = 0; pr < P_S / 2; ++pr) mbar_init(empty(pr), 1);
-    for (int r = 0; r < 2; ++r) {
-      mbar_init(accfull(r), 1);
-      mbar_init(accempty(r), EPI_WARPS + 1);  // leader: own warps + the peer's forward
-      mbar_init(accfree(r), EPI_WARPS);       // peer: its epilogue warps
-      mbar_init(saready(r), EPI_THREADS);
-    }
-    mbar_init(drain_bar, 1);
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0 && lane == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
-  }
-  if (warp == 1) {
-    // one warp of each CTA of the pair allocates collectively
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(512));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
-  }
-  tc_fence_before();
-  cluster_sync_all();  // both CTAs' barriers initialised, TMEM allocated
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int nkb = p.nkb, chunk_kb = p.chunk_kb;
-
-  if (warp >= 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
-    if (rank == 0) {
-      epilogue_role<PERGROUP, P_BT, true>(p, tmem, base, sm, P_OFF_SA, warp, lane, pair0, npairs,
-                                          nblocks2, 2 * BW, 0, accfull(0), accempty(0),
-                                          saready(0), abort_flag);
-    } else {
-      epilogue_role<PERGROUP, P_BT, true>(p, tmem, base, sm, P_OFF_SA, warp, lane, pair0, npairs,
-                                          nblocks2, 2 * BW, BW, accfull(0), accfree(0),
-                                          saready(0), abort_flag, map_to_rank(accempty(0), 0));
-    }
-  } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;");
-    if (warp == 0) {
-      // ------------------------------------ weight staging TMA producer --
-      if (lane == 0) {
-        int s8 = 0;
-        uint32_t ph8 = 0, pend = 0, pph = 0;
-        const uint32_t bytes8 = WBITS == 8 ? P_W8_BYTES : P_W8_BYTES / 2;
-        bool ok = true;
-        for (int tile = pair0; tile < p.ntiles && ok; tile += npairs) {
-          const int nb = tile % nblocks2;
-          const int row0 = nb * 2 * BW + static_cast<int>(rank) * BW;
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bar(empty8(s8), ph8 ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(full8(s8), bytes8);
-            tma_load_2d(base + P_OFF_W8 + s8 * P_W8_BYTES, &tmW, full8(s8),
-                        WBITS == 8 ? kb * BK : kb * (BK / 2), row0);
-            pend |= 1u << s8;
-            pph = (pph & ~(1u << s8)) | (ph8 << s8);
-            if (++s8 == P_S8) {
-              s8 = 0;
-              ph8 ^= 1u;
-            }
-          }
-        }
-        for (int i = 0; i < P_S8; ++i)
-          if ((pend >> i) & 1u) wait_bar_teardown(full8(i), (pph >> i) & 1u);
-      }
-    } else if (warp == 2) {
-      // ------------------------- activation (fp16 codes) TMA producer --
-      if (lane == 0) {
-        int s = 0;
-        uint32_t ph = 0, pend = 0, pph = 0;
-        bool ok = true;
-        for (int tile = pair0; tile < p.ntiles && ok; tile += npairs) {
-          const int tb = tile / nblocks2;
-          const int tok0 = tb * P_BT + static_cast<int>(rank) * (P_BT / 2);
-          for (int kb = 0; kb < nkb; ++kb) {
-            // a stage pair is refilled once the MMAs of its last use are done
-            if ((s & 1) == 0 &&
-                !wait_bar_cluster(empty(s >> 1), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(xfull(s), P_X16_BYTES);
-            tma_load_2d(base + P_OFF_X16 + s * P_X16_BYTES, &tmX, xfull(s), kb * BK, tok0);
-            pend |= 1u << s;
-            pph = (pph & ~(1u << s)) | (ph << s);
-            if (++s == P_S) {
-              s = 0;
-              ph ^= 1u;
-            }
-          }
-        }
-        for (int i = 0; i < P_S; ++i)
-          if ((pend >> i) & 1u) wait_bar_teardown(xfull(i), (pph >> i) & 1u);
-      }
-    } else if (warp == 1) {
-      // ---------------------------------------- MMA issuer (leader CTA) --
-      if (lane == 0 && rank == 0) {
-        int s = 0;
-        uint32_t ph = 0, cc = 0;
-        bool ok = true;
-        for (int tile = pair0; tile < p.ntiles && ok; tile += npairs) {
-          for (int kb = 0; kb < nkb; ++kb) {
-            const bool first = (kb % chunk_kb) == 0;
-            const uint32_t r = cc & 1u;
-            if (first) {
-              if (!wait_bar_cluster(accempty(r), ((cc >> 1) & 1u) ^ 1u, abort_flag,
-                                    kDevErrTmemEmpty, p.err)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-            }
-            if (!wait_bar_cluster(full(s), ph, abort_flag, kDevErrFullBarrier, p.err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem + r * P_BT;
-            const uint32_t w_base = base + P_OFF_W16 + s * P_W16_BYTES;
-            const uint32_t x_base = base + P_OFF_X16 + s * P_X16_BYTES;
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              tc2_mma(d, sw128_desc(w_base + k * 32), sw128_desc(x_base + k * 32),
-                      (first && k == 0) ? 0u : 1u);
-            }
-            if (s & 1) tc2_commit_both(empty(s >> 1));
-            if ((kb % chunk_kb) == chunk_kb - 1 || kb == nkb - 1) {
-              tc2_commit_both(accfull(r));
-              ++cc;
-            }
-            if (++s == P_S) {
-              s = 0;
-              ph ^= 1u;
-            }
-          }
-        }
-        // release a half-used final pair too, then let every MMA land
-        if (s & 1) tc2_commit_both(empty(s >> 1));
-        tc2_commit_both(drain_bar);
-        wait_bar_teardown(drain_bar, 0);
-      } else if (lane == 0) {
-        // ------------------------------- stage forwarder (non-leader CTA) --
-        // once this CTA's converter warps have finished a stage (each after
-        // seeing its activation copy land), one cluster-scope arrive tells the
-        // leader
-        const uint32_t full_leader = map_to_rank(full(0), 0);
-        int s = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int tile = pair0; tile < p.ntiles && ok; tile += npairs) {
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bar(wfull(s), ph, abort_flag, kDevErrFullBarrier, p.err)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_cluster(full_leader + 8u * s);
-            if (++s == P_S) {
-              s = 0;
-              ph ^= 1u;
-            }
-          }
-        }
-      }
-    } else {
-      // --------------------------------------------------- converters ----
-      constexpr int NT = P_CONV_WARPS * 32;
-      const int ct = (warp - P_CONV_WARP0) * 32 + lane;
-      int s8 = 0, s = 0;
-      uint32_t ph8 = 0, ph = 0;
-      bool ok = true;
-      for (int tile = pair0; tile < p.ntiles && ok; tile += npairs) {
-        for (int kb = 0; kb < nkb; ++kb) {
-          bool w = wait_bar(full8(s8), ph8, abort_flag, kDevErrFullBarrier, p.err);
-          if ((s & 1) == 0)
-            w = w && wait_bar_cluster(empty(s >> 1), ph ^ 1u, abort_flag, kDevErrEmptyBarrier,
-                                      p.err);
-          if (!__all_sync(0xffffffffu, w)) {
-            ok = false;
-            break;
-          }
-          convert_tile<WBITS == 4, NT>(sm + P_OFF_W8 + s8 * P_W8_BYTES,
-                                       sm + P_OFF_W16 + s * P_W16_BYTES, BW, ct);
-          // the stage is complete once this CTA's activation copy has landed too
-          // (waited only now, so the conversion overlaps the copy)
-          if (!__all_sync(0xffffffffu,
-                          wait_bar(xfull(s), ph, abort_flag, kDevErrFullBarrier, p.err))) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            // this CTA's weights converted and its activations landed: the
-            // leader's own stage barrier, or the local one the forwarder watches
-            mbar_arrive(rank == 0 ? full(s) : wfull(s));
-            mbar_arrive(empty8(s8));
-          }
-          if (++s8 == P_S8) {
-            s8 = 0;
-            ph8 ^= 1u;
-          }
-          if (++s == P_S) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-    }
-  }
-
-  __syncwarp();
-  tc_fence_before();
-  cluster_sync_all();  // no more traffic between the two CTAs after this
-  tc_fence_after();
-  if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
 }
 
@@ -1224,75 +831,16 @@ int launch_modes(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p
   return launch_t<8, false, XH, BT>(tx, tw, p, s);
 }
 
-template <int WBITS, bool PERGROUP>
-int launch_pair_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p,
-                  cudaStream_t s) {
-  static bool attr_set[64] = {};
-  static int sms[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return W8A8_ERR_CUDA;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_tc2_kernel<WBITS, PERGROUP>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             P_SMEM_BYTES) != cudaSuccess)
-      return W8A8_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return W8A8_ERR_CUDA;
-    attr_set[dev] = true;
-  }
-  const int pairs = p.ntiles < sms[dev] / 2 ? p.ntiles : sms[dev] / 2;
-  // the cluster shape (2, 1, 1) is part of the kernel
-  gemm_tc2_kernel<WBITS, PERGROUP><<<2 * pairs, NUM_THREADS, P_SMEM_BYTES, s>>>(tx, tw, p);
-  return launch_status();
-}
-
 }  // namespace
 
-// The CTA-pair GEMM for fp16 activation codes: 256 channels x 256 tokens per
-// pair tile.
-int launch_gemm_tc_pair(const void *X, const float *sa, const void *W, const float *sw, int M,
-                        int N, int K, int group_size, int wbits, __half *y, cudaStream_t s) {
-  CUtensorMap tx, tw;
-  if (!make_map(&tx, X, M, K, 2, P_BT / 2, BK)) return W8A8_ERR_CUDA;
-  if (wbits == 8) {
-    if (!make_map(&tw, W, N, K, 1, BW, BK)) return W8A8_ERR_CUDA;
-  } else {
-    if (!make_map(&tw, W, N, K / 2, 1, BW, BK / 2)) return W8A8_ERR_CUDA;
-  }
-  unsigned int *err = device_error_word();
-  if (err == nullptr) return W8A8_ERR_CUDA;
-  TcParams p;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.gs = group_size;
-  p.G = groups_of(K, group_size);
-  p.nkb = (K + BK - 1) / BK;
-  if (group_size != 0)
-    p.chunk_kb = group_size / BK;
-  else
-    p.chunk_kb = wbits == 8 ? 1024 / BK : 16384 / BK;
-  p.nblocks = (N + 2 * BW - 1) / (2 * BW);  // 256-channel blocks
-  const long tblocks = (M + P_BT - 1) / P_BT;
-  const long ntiles = static_cast<long>(p.nblocks) * tblocks;
-  if (ntiles > 0x7fffffffL) return W8A8_ERR_INVALID_ARG;
-  p.ntiles = static_cast<int>(ntiles);
-  p.sa = sa;
-  p.sw = sw;
-  p.y = y;
-  p.acc_out = nullptr;
-  p.err = err;
-  if (wbits == 4) return launch_pair_t<4, false>(tx, tw, p, s);
-  if (group_size != 0) return launch_pair_t<8, true>(tx, tw, p, s);
-  return launch_pair_t<8, false>(tx, tw, p, s);
-}
-
 // X (activations) is int8 codes [M, K] (x_half false) or the same codes as
-// fp16 values (x_half true).  128-token tiles when M <= 128, else 256.
+// fp16 values (x_half true).  256-token tiles for fp16 codes with M > 128,
+// else 128.
 int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, const float *sw,
                    int M, int N, int K, int group_size, int wbits, __half *y,
                    int32_t *acc_out, cudaStream_t s) {
-  const int bt = M <= 128 ? 128 : 256;
+  // INT8 activation codes are converted in the kernel too: 128-token tiles
+  const int bt = (M <= 128 || !x_half) ? 128 : 256;
   CUtensorMap tx, tw;
   if (!make_map(&tx, X, M, K, x_half ? 2 : 1, bt, BK)) return W8A8_ERR_CUDA;
   if (wbits == 8) {
@@ -1327,8 +875,7 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
   if (x_half)
     return bt == 128 ? launch_modes<true, 128>(tx, tw, p, wbits, s)
                      : launch_modes<true, 256>(tx, tw, p, wbits, s);
-  return bt == 128 ? launch_modes<false, 128>(tx, tw, p, wbits, s)
-                   : launch_modes<false, 256>(tx, tw, p, wbits, s);
+  return launch_modes<false, 128>(tx, tw, p, wbits, s);
 }
 
 }  // namespace w8a8
