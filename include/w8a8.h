@@ -177,6 +177,25 @@ int linear(const w8a8_half *x, const void *Wq, const float *scale_w, int M,
            int N, int K, int group_size, int wbits, void *workspace,
            size_t ws_bytes, w8a8_half *y, w8a8_stream_t stream);
 
+/* linear() with no workspace argument, for callers that cannot allocate
+ * device memory on their execution path (for example a serving runtime's
+ * per-request path, where cudaMalloc may synchronize the device and fail
+ * under memory pressure, or a plugin inside a host framework that owns all
+ * device memory and exposes no allocator).  No counterpart on the method's
+ * pages: an addition of this library.
+ *   Arguments as linear(), minus workspace / ws_bytes.  The workspace is a
+ *   fixed 8 MiB array in the library's device memory (held by every GPU that
+ *   loads the library until the process exits); a problem whose
+ *   w8a8_linear_workspace_bytes(M, K, group_size) exceeds 8 MiB returns
+ *   W8A8_ERR_WORKSPACE and touches nothing.  Calls no allocator.
+ *   All calls on a device share the array: calls whose kernels overlap on
+ *   the GPU (unordered streams) race; calls on one stream are safe.  The
+ *   first call on a device looks up the array's address, once per device;
+ *   make it before any stream capture begins. */
+int linear_noalloc(const w8a8_half *x, const void *Wq, const float *scale_w, int M,
+                   int N, int K, int group_size, int wbits, w8a8_half *y,
+                   w8a8_stream_t stream);
+
 /* Test export of step 3 alone ("INT8 TensorOps 커널 설계": INT32
  * accumulation): acc[m, n, g] = sum over k in group g of xq[m, k] *
  * Wq[n, k], exact, as int32 [M, N, G], through the same tensor-core

@@ -29,7 +29,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or K",
 EXPORTS = ("w8a8_is_available", "w8a8_status_string", "w8a8_check_status",
            "quantize_weight_int8", "pack_weight_int4", "quantize_act_per_token",
            "w8a8_gemm", "w8a8_mv", "w4a8_gemm", "quantize_act_per_token_h", "w8a8_gemm_h",
-           "w8a8_linear_workspace_bytes", "linear", "w8a8_gemm_i32")
+           "w8a8_linear_workspace_bytes", "linear", "linear_noalloc", "w8a8_gemm_i32")
 
 
 class W8A8Error(RuntimeError):
@@ -64,6 +64,7 @@ def load(path: str | None = None):
             "w8a8_gemm_h": ([P, P, P, P, I, I, I, I, I, P, P], I),
             "w8a8_linear_workspace_bytes": ([I, I, I], Z),
             "linear": ([P, P, P, I, I, I, I, I, P, Z, P, P], I),
+            "linear_noalloc": ([P, P, P, I, I, I, I, I, P, P], I),
             "w8a8_gemm_i32": ([P, P, I, I, I, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
@@ -260,6 +261,24 @@ def linear(x, Wq, scale_w, group_size: int = 0, wbits: int = 8, workspace=None, 
     _need(y, torch.float16, "y", (M, N))
     _check(load().linear(_ptr(x), _ptr(Wq), _ptr(scale_w), M, N, K, group_size, wbits,
                          _ptr(workspace), workspace.numel(), _ptr(y), _stream()), "linear")
+    return y
+
+
+def linear_noalloc(x, Wq, scale_w, group_size: int = 0, wbits: int = 8, y=None):
+    """linear() without a workspace: the library's fixed 8 MiB device array
+    serves as the workspace, so the C call allocates nothing (the output is
+    allocated here if not given).  Problems that do not fit raise W8A8Error
+    (status 6).  Calls on streams that overlap on the GPU race on the array."""
+    _need(x, torch.float16, "x")
+    M, K = x.shape
+    wdtype = torch.int8 if wbits == 8 else torch.uint8
+    _need(Wq, wdtype, "Wq")
+    N = Wq.shape[0]
+    _need(scale_w, torch.float32, "scale_w", (N, _groups(K, group_size)))
+    y = torch.empty((M, N), dtype=torch.float16, device=x.device) if y is None else y
+    _need(y, torch.float16, "y", (M, N))
+    _check(load().linear_noalloc(_ptr(x), _ptr(Wq), _ptr(scale_w), M, N, K, group_size, wbits,
+                                 _ptr(y), _stream()), "linear_noalloc")
     return y
 
 
