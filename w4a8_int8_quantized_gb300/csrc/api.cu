@@ -250,11 +250,9 @@ int linear(const w8a8_half *x, const void *Wq, const float *scale_w, int M,
   float *sa = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                         round256(static_cast<size_t>(M) * K * code_bytes));
   if (M == 1) {
-    int8_t *xq = static_cast<int8_t *>(workspace);
-    W8A8_TRY(launch_row_quant(reinterpret_cast<const __half *>(x), M, K, group_size, 127, xq,
-                              nullptr, sa, s));
-    return gemm_dispatch(xq, sa, Wq, scale_w, M, N, K, group_size, wbits,
-                         reinterpret_cast<__half *>(y), s);
+    // decode: one kernel quantizes the row and streams the weights
+    return launch_linear_mv(reinterpret_cast<const __half *>(x), Wq, scale_w, N, K, group_size,
+                            wbits, reinterpret_cast<__half *>(y), s);
   }
   __half *xq_h = static_cast<__half *>(workspace);
   W8A8_TRY(launch_row_quant_half(reinterpret_cast<const __half *>(x), M, K, group_size, xq_h,

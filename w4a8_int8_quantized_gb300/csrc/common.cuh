@@ -69,6 +69,9 @@ int launch_gemv_w8a8(const int8_t *xq, const float *sa, const int8_t *Wq,
                      cudaStream_t s);
 int launch_gemv_w4a8(const int8_t *xq, const float *sa, const uint8_t *Wp,
                      const float *sw, int N, int K, __half *y, cudaStream_t s);
+// The whole layer for one fp16 row: quantization fused into the MV kernel.
+int launch_linear_mv(const __half *x, const void *W, const float *sw, int N, int K,
+                     int group_size, int wbits, __half *y, cudaStream_t s);
 
 // Row quantization writing the INT8 codes as fp16 values.
 int launch_row_quant_half(const __half *x, int R, int K, int group_size, __half *qh,

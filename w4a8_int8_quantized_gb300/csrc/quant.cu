@@ -8,8 +8,8 @@
 // "cider의 양자화 모드와 적용 가능한 영역" (symmetric INT8 per token; INT4
 // weights packed two per uint8 for W4A8).
 //
-// Design (HBM-bound, one streaming pass): a team of T threads (one warp for
-// K <= 4096, up to 256 threads for K <= 32768) owns one row.  Each thread
+// Design (HBM-bound, one streaming pass): a team of T threads (32 to 256,
+// so that each thread caches at most 4 vectors where K allows) owns one row.  Each thread
 // loads its V 16-byte vectors (8 fp16 each) once into registers, the team
 // reduces absmax with warp shuffles (and shared memory when T > 32), and the
 // same registers are quantized and stored.  Vector i of thread t covers
@@ -22,39 +22,14 @@
 // stores; the operand format of the tensor-core GEMM, every code being an
 // fp16 integer exactly), or INT4 codes packed two per byte.
 //
-// Rounding: q = clamp(rint(x / s), -qmax, qmax) with x / s one IEEE fp32
-// division.  The kernel evaluates t = x * (1/s) with a correctly rounded
-// reciprocal: |t - x/s| <= |x/s| (2^-23 + 2^-48) and the IEEE quotient is
-// within |x/s| 2^-24 of x/s, so with |x/s| <= 127.01 the two differ by less
-// than 2.3e-5.  When t is farther than 2^-14 from every half-integer, both
-// lie strictly on the same side of the same half-integer and round to the
-// same integer; only the rare t within 2^-14 of a half-integer takes the
-// IEEE division itself.  The result is bit-identical to the plain rule.
+// Rounding: see quant_rule.cuh.
 #include "common.cuh"
+#include "quant_rule.cuh"
 
 namespace w8a8 {
 namespace {
 
 enum OutMode { kOutInt8 = 0, kOutHalf = 1, kOutInt4 = 2 };
-
-__device__ __forceinline__ float absmax8(const uint4 &v) {
-  const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-  __half2 m = __habs2(h[0]);
-  m = __hmax2(m, __habs2(h[1]));
-  m = __hmax2(m, __habs2(h[2]));
-  m = __hmax2(m, __habs2(h[3]));
-  return fmaxf(__low2float(m), __high2float(m));
-}
-
-// q = clamp(rint(x / s), -qmax, qmax): see the rounding note above.
-__device__ __forceinline__ int quant1(float x, float s, float rcp, int qmax) {
-  const float t = __fmul_rn(x, rcp);
-  float r = rintf(t);
-  const float to_half = 0.5f - fabsf(t - r);  // distance to the nearest half-integer
-  if (to_half <= 6.103515625e-05f) r = rintf(__fdiv_rn(x, s));
-  const int q = static_cast<int>(r);
-  return max(-qmax, min(qmax, q));
-}
 
 template <int V, int MODE>
 __global__ void __launch_bounds__(256) row_quant_kernel(
@@ -172,8 +147,10 @@ template <int MODE>
 int launch_mode(const __half *x, int R, int K, int group_size, int qmax, void *out,
                 float *scale, cudaStream_t s) {
   const int nvec = K >> 3;
+  // enough threads per row that each caches at most 4 vectors (more warps
+  // resident per SM), up to 256; beyond that up to 16 vectors per thread
   int T = 32;
-  while (T < 256 && (nvec + T - 1) / T > 16) T <<= 1;
+  while (T < 256 && (nvec + T - 1) / T > 4) T <<= 1;
   const int V = (nvec + T - 1) / T;
   switch (V) {
 #define W8A8_CASE(n) \
