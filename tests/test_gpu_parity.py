@@ -230,7 +230,9 @@ def test_gemm_with_half_codes(M, N, K, gs, wbits):
 
 
 @pytest.mark.parametrize("N,K,gs", [(257, 512, 0), (10240, 2560, 0), (130, 2560, 64),
-                                    (300, 4096, 128), (4096, 14336, 0), (1, 16, 0)])
+                                    (300, 4096, 128), (4096, 14336, 0), (1, 16, 0),
+                                    (700, 48, 0), (5, 32768, 0), (33, 64, 64), (9, 32768, 64),
+                                    (3000, 32768, 64), (1001, 640, 128)])
 def test_w8a8_mv_output(N, K, gs):
     x = act(1, K, seed=N + 1, n_outliers=2, outlier_scale=30.0)
     W = synth.weights(N, K, seed=N + 2)
@@ -244,7 +246,7 @@ def test_w8a8_mv_output(N, K, gs):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 257, 512), (1, 14336, 4096), (130, 257, 512),
-                                   (257, 129, 4096), (2, 64, 32)])
+                                   (257, 129, 4096), (2, 64, 32), (1, 700, 32), (1, 7, 32768)])
 def test_w4a8_gemm_output(M, N, K):
     x = act(M, K, seed=M + 5)
     W = synth.weights(N, K, seed=N + 5)
@@ -260,7 +262,8 @@ def test_w4a8_gemm_output(M, N, K):
 
 @pytest.mark.parametrize("M,N,K,gs,wbits", [
     (1, 512, 512, 0, 8), (128, 512, 512, 0, 8), (5, 300, 2560, 128, 8), (1, 300, 2560, 64, 8),
-    (300, 257, 4096, 0, 4), (1, 257, 4096, 0, 4)])
+    (300, 257, 4096, 0, 4), (1, 257, 4096, 0, 4), (1, 40, 32768, 64, 8), (1, 1000, 16, 0, 8),
+    (1, 333, 96, 0, 4)])
 def test_linear_matches_oracle(M, N, K, gs, wbits):
     x = act(M, K, seed=3, n_outliers=4, outlier_scale=40.0)
     W = synth.weights(N, K, seed=4)
