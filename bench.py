@@ -16,7 +16,14 @@ e2e      = the same metric through the C ABI's ``linear`` call with pinned
            of y, all inside the timed events.
 roofline = the dominant kernel (the GEMM at M=8192): 2*M*N*K / its average
            CUDA-event duration over the timed steps, against the measured
-           dense fp16/bf16 tensor peak.
+           dense fp16/bf16 tensor peak; traffic = DRAM bytes per launch from
+           the committed ncu summary of that kernel, while its source is
+           unchanged since the capture.
+decode   = the decode matrix-vector path (M = 1) timed the way decode runs,
+           layer after layer: back-to-back linear() calls over R distinct
+           copies of the weights (R x 26 MB > 2 x L2), so every call streams
+           its weights from HBM; GB/s = algorithmic bytes per call (INT8
+           weights, their scales, x, y) / time per call.
 cpu_baseline / --impl reference = the CPU oracle, as it stands, on a bounded
            sample of rows of the same workload.
 """
@@ -30,6 +37,8 @@ import subprocess
 import sys
 import threading
 import time
+
+import hashlib
 
 import numpy as np
 
@@ -47,6 +56,29 @@ UNIT = "TOPS"
 PAGES_MS = {1: 0.27, 128: 0.34, 1024: 1.23, 4096: 4.41, 8192: 8.71}
 PAGES_TOPS = sum(2.0 * m * N_OUT * K_IN for m in MS) / (sum(PAGES_MS.values()) * 1e-3) / 1e12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_m8192_n10240_k2560.txt")
+GEMM_SOURCE = os.path.join(ROOT, "w4a8_int8_quantized_gb300", "csrc", "gemm_tc.cu")
+
+
+def gemm_traffic():
+    """DRAM bytes per launch of the GEMM at M=8192 from the committed ncu
+    summary, or None when the kernel source changed since that capture."""
+    try:
+        fields = {}
+        with open(GEMM_PROFILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        with open(GEMM_SOURCE, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if fields.get("gemm_tc.cu sha256") != sha:
+            return None
+        return float(fields["dram bytes per launch"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def config_dict():
@@ -409,6 +441,44 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e2e_ms, ws, device)
     e2e_value = ws * step_ops() / (e2e_ms * 1e-3) / 1e12
 
+    # decode, back to back over distinct weight copies
+    decode = None
+    if rank == 0 and not args.no_decode:
+        n_copies = max(4, int(3 * l2 // (N_OUT * K_IN)) + 1)
+        copies = [wq.clone() for _ in range(n_copies)]
+        b1 = bufs[1]
+
+        def decode_round():
+            for c in copies:
+                check(lib.linear(P(b1["x"].data_ptr()), P(c.data_ptr()), P(sw.data_ptr()), 1,
+                                 N_OUT, K_IN, 0, 8, P(b1["ws"].data_ptr()), b1["ws"].numel(),
+                                 P(b1["y"].data_ptr()), s_ptr), "decode")
+
+        for _ in range(3):
+            decode_round()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(max(10, min(args.steps, 100))):
+            torch.cuda._sleep(int(1e6))
+            e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            e0.record(stream)
+            decode_round()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / n_copies)
+        us = statistics.median(times)
+        dbytes = N_OUT * K_IN + N_OUT * 4 + K_IN * 2 + N_OUT * 2
+        hbm = _peak(peaks, "hbm_gbs") if peak_src == "measured" else None
+        hbm_src = peak_src if hbm is not None else "fallback"
+        hbm = hbm if hbm is not None else FALLBACK_PEAKS["hbm_gbs"]
+        decode = {"us_per_call": round(us, 3), "GBps": round(dbytes / (us * 1e-6) / 1e9, 1),
+                  "bytes_per_call": dbytes, "hbm_peak_gbs": hbm,
+                  "frac_of_hbm": round(dbytes / (us * 1e-6) / 1e9 / hbm, 4),
+                  "peak_source": f"{hbm_src} HBM copy bandwidth",
+                  "method": f"back-to-back linear() calls, M=1, over {n_copies} distinct weight "
+                            f"copies; median of {len(times)} rounds"}
+        del copies
+
     detail = {}
     for m in MS:
         q = per_m[m]["quant_ms"] / args.steps
@@ -433,7 +503,7 @@ def run_ours(args):
     if peak is None:
         peak, peak_src = FALLBACK_PEAKS["bf16_tflops"], "fallback"
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": gemm_traffic(),
                 "kernel": f"w8a8 GEMM, M={mdom}, N={N_OUT}, K={K_IN}",
                 "peak_source": f"{peak_src} dense bf16/fp16 tensor peak (burst)"}
 
@@ -446,7 +516,7 @@ def run_ours(args):
                     "h2d_bytes_per_step": sum(m * K_IN * 2 for m in MS),
                     "d2h_bytes_per_step": sum(m * N_OUT * 2 for m in MS)},
             "gpu_launches": args.steps * (2 * len(MS) - 1),  # M=1 is one fused launch
-            "clocks": clocks.summary(), "detail": detail,
+            "clocks": clocks.summary(), "decode": decode, "detail": detail,
             "wall_s_timed_region": round(wall, 4)}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inputs)
@@ -512,6 +582,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU-oracle sample (about 15 s)")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the back-to-back decode measurement")
     ap.add_argument("--only", choices=["quant", "quant_i8", "gemm", "gemm_i8", "w4a8", "linear",
                                        "linear4"],
                     help="run one kernel of the path on one shape (for profilers)")
