@@ -245,7 +245,7 @@ def calibrate_rows(inputs, target_s):
     return max(2, min(want, 8192)), t
 
 
-def cpu_baseline(inputs, target_s=12.0):
+def cpu_baseline(inputs, target_s=20.0):
     import oracle
     oracle.build()
     wq, sw = oracle.quantize_weight_int8(inputs["W"])

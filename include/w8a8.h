@@ -121,9 +121,17 @@ int w8a8_gemm(const int8_t *xq, const float *scale_a, const int8_t *Wq,
               const float *scale_w, int M, int N, int K, int group_size,
               w8a8_half *y, w8a8_stream_t stream);
 
-/* W8A8 matrix-vector product for decode (the SDK's INT8 MV kernel,
- * "cider 소개", seq_len == 1; per channel or per group).  Same arguments as
- * w8a8_gemm; M must be 1 (else W8A8_ERR_INVALID_ARG). */
+/* W8A8 matrix-vector product for decode (the SDK's INT8 MV kernel for
+ * seq_len == 1, "cider 소개", section "cider의 동작 방식과 자동 경로 선택";
+ * per channel or per group).  Same arguments as w8a8_gemm; M must be 1 (else
+ * W8A8_ERR_INVALID_ARG).
+ * Ordering: the matrix-vector kernel is launched with programmatic stream
+ * serialization, and it may start reading Wq (only Wq) before the previous
+ * kernel on the stream has finished when that kernel lets its dependents
+ * start early (executes griddepcontrol.launch_dependents).  Do not write Wq
+ * in such a kernel right before this call; the library's own kernels that
+ * write weights never let dependents start early.  The same holds for
+ * w4a8_gemm and linear with M == 1. */
 int w8a8_mv(const int8_t *xq, const float *scale_a, const int8_t *Wq,
             const float *scale_w, int M, int N, int K, int group_size,
             w8a8_half *y, w8a8_stream_t stream);
@@ -162,11 +170,13 @@ int w8a8_gemm_h(const w8a8_half *xq_h, const float *scale_a, const void *Wq,
  * scales, each region 256-byte aligned. */
 size_t w8a8_linear_workspace_bytes(int M, int K, int group_size);
 
-/* The whole layer, CiderLinear's forward ("cider 소개": seq_len > 1 ->
- * INT8 GEMM, seq_len == 1 -> INT8 MV kernel): quantize x per token into
- * the workspace (quantize_act_per_token_h for M > 1, quantize_act_per_token
- * for M == 1), then run the GEMM (w8a8_gemm_h) or the matrix-vector kernel
- * with the fused dequant.
+/* The whole layer, CiderLinear's forward ("cider 소개", section "cider의
+ * 동작 방식과 자동 경로 선택": seq_len > 1 -> INT8 GEMM, seq_len == 1 ->
+ * INT8 MV kernel).  M > 1: quantize x per token into the workspace
+ * (quantize_act_per_token_h), then the GEMM (w8a8_gemm_h) with the fused
+ * dequant.  M == 1: one kernel quantizes the row (same rule) and runs the
+ * matrix-vector product with the fused dequant; the workspace is checked
+ * but not written (see w8a8_mv for the ordering rule of that kernel).
  *   x        fp16 [M, K]
  *   Wq       int8 [N, K] (wbits 8) or packed uint8 [N, K/2] (wbits 4)
  *   scale_w  fp32 [N, G] (wbits 4 requires group_size 0)

@@ -1,10 +1,11 @@
 // Decode-path matrix-vector kernels (M == 1): W8A8 per channel / per group,
 // and W4A8 per channel; optionally fused with the activation quantization.
 //
-// Method: "cider 소개", section "cider의 성능 측정 결과" (CiderLinear picks
-// the INT8 MV kernel when seq_len == 1) and the kernel list in the same page
-// (w8a8_int8_mv, pergroup_int8_mv); "Apple Silicon의 AI 한계치는 당신의
-// 생각보다 높습니다", section "INT8 TensorOps 커널 설계", steps 1-4.
+// Method: "cider 소개", section "cider의 동작 방식과 자동 경로 선택"
+// (CiderLinear picks the INT8 MV kernel when seq_len == 1; the kernel list
+// names a per-channel and a per-group MV kernel); "Apple Silicon의 AI
+// 한계치는 당신의 생각보다 높습니다", section "INT8 TensorOps 커널 설계",
+// steps 1-4.
 //
 // Design (HBM-bound: the weight matrix is read once, as a flat stream).
 //  * Each CTA owns a contiguous range of weight rows -- one contiguous range
