@@ -71,7 +71,9 @@ struct Plan {
   static constexpr int W16_BYTES = BW * BK * 2;    // fp16 operands, 128-byte rows
   static constexpr int X16_BYTES = BT * BK * 2;
   static constexpr int STAGE_BYTES = W16_BYTES + X16_BYTES;
-  static constexpr int S8 = 3, S = 4;               // S: operand stages
+  // S: operand stages.  A fourth measured no faster, and three leave more of
+  // the SM's L1 to the per-group epilogue's scale loads.
+  static constexpr int S8 = 3, S = 3;
 #ifndef W8A8_TC_RELEASE
   static constexpr int REL = 1;                    // stages released per commit
 #else
@@ -307,48 +309,46 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int j) {
 // load (8 bytes of packed INT4) and two 16-byte stores into swizzled chunks
 // 2 (u % 4) and 2 (u % 4) + 1.  A warp covers 8 whole rows; each 8-thread
 // store phase writes two rows' even (or odd) chunks, which the 128-byte
-// swizzle puts in disjoint banks.  Two units per thread are loaded before
-// either is converted.
-template <bool INT4, int NT>
-__device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, int rows,
-                                             int ct) {
-  const int units = rows * 4;
-#pragma unroll 1
-  for (int u0 = ct; u0 < units; u0 += 2 * NT) {
-    uint4 v[2];
+// swizzle puts in disjoint banks.  All of a thread's units (UPT of them) are
+// loaded before any is converted, so a tile costs one shared-memory round
+// trip per thread, not one per unit.
+template <bool INT4, int NT, int ROWS>
+__device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, int ct) {
+  constexpr int units = ROWS * 4;
+  constexpr int UPT = (units + NT - 1) / NT;  // units per thread
+  uint4 v[UPT];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int u = u0 + i * NT;
-      v[i] = make_uint4(0, 0, 0, 0);
-      if (u < units) {
-        const int r = u >> 2, c = u & 3;
-        if (INT4) {
-          const uint2 w = *reinterpret_cast<const uint2 *>(src + r * 32 + c * 8);
-          v[i].x = w.x;
-          v[i].y = w.y;
-        } else {
-          v[i] = *reinterpret_cast<const uint4 *>(src + r * 64 + c * 16);
-        }
+  for (int i = 0; i < UPT; ++i) {
+    const int u = ct + i * NT;
+    v[i] = make_uint4(0, 0, 0, 0);
+    if (u < units) {
+      const int r = u >> 2, c = u & 3;
+      if (INT4) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(src + r * 32 + c * 8);
+        v[i].x = w.x;
+        v[i].y = w.y;
+      } else {
+        v[i] = *reinterpret_cast<const uint4 *>(src + r * 64 + c * 16);
       }
     }
+  }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int u = u0 + i * NT;
-      if (u < units) {
-        const int r = u >> 2, c = u & 3;
-        uint4 lo, hi;
-        if (INT4) {
-          lo = i4x8_to_h(v[i].x);
-          hi = i4x8_to_h(v[i].y);
-        } else {
-          lo = i8x8_to_h(make_uint2(v[i].x, v[i].y));
-          hi = i8x8_to_h(make_uint2(v[i].z, v[i].w));
-        }
-        uint8_t *row = dst + (r >> 3) * 1024 + (r & 7) * 128;
-        const int x = r & 7;
-        *reinterpret_cast<uint4 *>(row + (((2 * c) ^ x) << 4)) = lo;
-        *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ x) << 4)) = hi;
+  for (int i = 0; i < UPT; ++i) {
+    const int u = ct + i * NT;
+    if (u < units) {
+      const int r = u >> 2, c = u & 3;
+      uint4 lo, hi;
+      if (INT4) {
+        lo = i4x8_to_h(v[i].x);
+        hi = i4x8_to_h(v[i].y);
+      } else {
+        lo = i8x8_to_h(make_uint2(v[i].x, v[i].y));
+        hi = i8x8_to_h(make_uint2(v[i].z, v[i].w));
       }
+      uint8_t *row = dst + (r >> 3) * 1024 + (r & 7) * 128;
+      const int x = r & 7;
+      *reinterpret_cast<uint4 *>(row + (((2 * c) ^ x) << 4)) = lo;
+      *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ x) << 4)) = hi;
     }
   }
 }
@@ -727,11 +727,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          convert_tile<WBITS == 4, NT>(sm + PL::OFF_W8 + s8 * PL::W8_BYTES,
-                                       sm + (w16(s) - base), BW, ct);
+          convert_tile<WBITS == 4, NT, BW>(sm + PL::OFF_W8 + s8 * PL::W8_BYTES,
+                                           sm + (w16(s) - base), ct);
           if (!XH)
-            convert_tile<false, NT>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES, sm + (x16(s) - base),
-                                    BT, ct);
+            convert_tile<false, NT, BT>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES,
+                                        sm + (x16(s) - base), ct);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
