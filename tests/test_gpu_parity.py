@@ -211,7 +211,7 @@ def test_w8a8_gemm_output(M, N, K, gs):
 @pytest.mark.parametrize("M,N,K,gs,wbits", [
     (130, 257, 512, 0, 8), (257, 130, 2560, 0, 8), (1, 300, 2560, 0, 8), (64, 96, 4096, 64, 8),
     (200, 257, 2560, 128, 8), (2, 3, 16, 0, 8), (129, 520, 14336, 0, 8), (300, 257, 4096, 0, 4),
-    (1, 129, 512, 0, 4)])
+    (1, 129, 512, 0, 4), (400, 300, 1024, 64, 8), (577, 129, 4096, 128, 8)])
 def test_gemm_with_half_codes(M, N, K, gs, wbits):
     """The GEMM fed with fp16 activation codes (the path linear uses for
     M > 1) gives the oracle's outputs bit for bit."""
