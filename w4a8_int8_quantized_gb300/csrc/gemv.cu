@@ -230,21 +230,11 @@ __global__ void __launch_bounds__(kThreads, 2 * kCtasPerSm) mv_kernel(
         if (v < nvec && (tid & ((gs >> 3) - 1)) == 0) ss[(v << 3) / gs] = s;
       }
       if (v < nvec) {
-        const __half2 *h = reinterpret_cast<const __half2 *>(&xvv);
-        uint32_t lo = 0, hi = 0;
+        float q[8];
+        quant_vec8(xvv, s, rcp, q);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(h[j]);
-          const int q0 = quant1(f.x, s, rcp, 127), q1 = quant1(f.y, s, rcp, 127);
-          asum += q0 + q1;
-          const uint32_t b = (static_cast<uint32_t>(q0) & 0xffu) |
-                             ((static_cast<uint32_t>(q1) & 0xffu) << 8);
-          if (j < 2)
-            lo |= b << (16 * j);
-          else
-            hi |= b << (16 * (j - 2));
-        }
-        reinterpret_cast<uint2 *>(xs)[v] = make_uint2(lo, hi);
+        for (int j = 0; j < 8; ++j) asum += __float2int_rn(q[j]);
+        reinterpret_cast<uint2 *>(xs)[v] = pack_i8x8(q);
       }
     }
   } else {

@@ -100,33 +100,25 @@ __global__ void __launch_bounds__(256) row_quant_kernel(
       if ((t & ((gs >> 3) - 1)) == 0) scale[r * G + g] = s;
     }
     // a zero row or group has s = 0 and rcp = 0: t = 0 and every code is 0
-    const __half2 *h = reinterpret_cast<const __half2 *>(&v[i]);
-    int qi[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float2 f = __half22float2(h[j]);
-      qi[2 * j] = quant1(f.x, s, rcp, qmax);
-      qi[2 * j + 1] = quant1(f.y, s, rcp, qmax);
-    }
+    float q[8];
+    quant_vec8(v[i], s, rcp, q);
     if (MODE == kOutInt8) {
-      uint32_t lo = (qi[0] & 0xff) | ((qi[1] & 0xff) << 8) |
-                    ((qi[2] & 0xff) << 16) | ((uint32_t)(qi[3] & 0xff) << 24);
-      uint32_t hi = (qi[4] & 0xff) | ((qi[5] & 0xff) << 8) |
-                    ((qi[6] & 0xff) << 16) | ((uint32_t)(qi[7] & 0xff) << 24);
-      reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + r * K)[vi] = make_uint2(lo, hi);
+      reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + r * K)[vi] = pack_i8x8(q);
     } else if (MODE == kOutHalf) {
+      // integral codes of magnitude <= 127 are fp16 values exactly; + 0
+      // turns a -0 code into +0, the fp16 value of the integer 0
       uint32_t w[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        __half2 hh = __halves2half2(__int2half_rn(qi[2 * j]), __int2half_rn(qi[2 * j + 1]));
-        w[j] = *reinterpret_cast<uint32_t *>(&hh);
+        const __half2 hh = __floats2half2_rn(q[2 * j] + 0.f, q[2 * j + 1] + 0.f);
+        w[j] = *reinterpret_cast<const uint32_t *>(&hh);
       }
       reinterpret_cast<uint4 *>(static_cast<__half *>(out) + r * K)[vi] =
           make_uint4(w[0], w[1], w[2], w[3]);
     } else {
       uint32_t w = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w |= (uint32_t)(qi[j] & 0xf) << (4 * j);
+      for (int j = 0; j < 8; ++j) w |= (static_cast<uint32_t>(__float2int_rn(q[j])) & 0xfu) << (4 * j);
       static_cast<uint32_t *>(out)[r * (K >> 3) + vi] = w;
     }
   }
