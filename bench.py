@@ -252,10 +252,12 @@ def cpu_baseline(inputs, target_s=20.0):
     inputs["wq_ref"], inputs["sw_ref"] = wq, sw
     rows, _ = calibrate_rows(inputs, target_s)
     ops, t = oracle_sample_step(rows, inputs)
+    what = ("every row of every M of the sweep" if rows >= max(MS)
+            else f"first {rows} rows of each M of the sweep")
     return {"value": ops / t / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"first {rows} rows of each M of the sweep (N=10240, K=2560) through "
-                      f"the oracle's quantize + int64 GEMM + dequant; {t:.1f} s"}
+            "sample": f"{what} (N=10240, K=2560) through the oracle's quantize + int64 GEMM "
+                      f"+ dequant; {t:.1f} s"}
 
 
 def run_reference(args):
