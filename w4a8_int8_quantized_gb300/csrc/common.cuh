@@ -29,6 +29,7 @@ enum DeviceErrorCode : unsigned int {
   kDevErrEmptyBarrier = 2,   // producer wait on a freed stage
   kDevErrAccumBarrier = 3,   // epilogue wait on a finished accumulator
   kDevErrTmemEmpty = 4,      // MMA wait on a drained accumulator
+  kDevErrSmemAlign = 5,      // dynamic shared memory not 1 KB aligned (kernel did nothing)
 };
 
 inline bool aligned16(const void *p) {

@@ -59,21 +59,32 @@ constexpr long long kTimeoutCycles = 4000000000LL;  // about 2 s at 2 GHz
 
 // Shared-memory plan.  XH: activations arrive as fp16 codes (TMA straight
 // into the operand layout); BT: tokens per tile (activations as INT8 codes
-// use BT = 128).  Two rings: the INT8 / INT4 staging ring (TMA ->
-// converters) and the operand stages, each holding one K block of fp16
-// weights (written by the converters) and fp16 activations (written by TMA,
-// or by the converters).  Operand stages are released REL at a time (one
-// MMA commit per REL K blocks).
-template <bool XH, int BT>
+// use BT = 128); KS: 64-wide K blocks per stage.  Two rings: the INT8 / INT4
+// staging ring (TMA -> converters) and the operand stages, each holding KS
+// K blocks of fp16 weights (written by the converters) and fp16 activations
+// (written by TMA, or by the converters), as KS 64-wide sub-tiles of
+// 128-byte swizzled rows per operand.  Operand stages are released REL at a
+// time (one MMA commit per REL stages).
+//
+// Every stage costs the same hand-offs between the roles (staging copy ->
+// converters -> MMA -> release), about 600 cycles of barrier round trips
+// measured with no data moved and no MMA issued, so KS = 2 (two K blocks
+// behind one hand-off, two stages of 96 KB) halves that cost per FLOP.  It
+// needs the full 227 KB, with no room for aligning the dynamic shared
+// memory by hand: the kernel checks that its base is 1 KB aligned instead.
+template <bool XH, int BT, int KS>
 struct Plan {
-  static constexpr int W8_BYTES = BW * BK;         // INT8 weight stage (INT4 uses half)
-  static constexpr int X8_BYTES = XH ? 0 : BT * BK;
-  static constexpr int W16_BYTES = BW * BK * 2;    // fp16 operands, 128-byte rows
-  static constexpr int X16_BYTES = BT * BK * 2;
+  static constexpr int KB = BK * KS;                // K per stage
+  static constexpr int W8_BYTES = BW * KB;          // INT8 weight stage (INT4 uses half)
+  static constexpr int X8_BYTES = XH ? 0 : BT * KB;
+  static constexpr int W16_SUB = BW * BK * 2;       // one fp16 sub-tile, 128-byte rows
+  static constexpr int X16_SUB = BT * BK * 2;
+  static constexpr int W16_BYTES = W16_SUB * KS;
+  static constexpr int X16_BYTES = X16_SUB * KS;
   static constexpr int STAGE_BYTES = W16_BYTES + X16_BYTES;
-  // S: operand stages.  A fourth measured no faster, and three leave more of
-  // the SM's L1 to the per-group epilogue's scale loads.
-  static constexpr int S8 = 3, S = 3;
+  // S: operand stages.  With KS = 1 a fourth measured no faster, and three
+  // leave more of the SM's L1 to the per-group epilogue's scale loads.
+  static constexpr int S8 = KS == 1 ? 3 : 2, S = KS == 1 ? 3 : 2;
 #ifndef W8A8_TC_RELEASE
   static constexpr int REL = 1;                    // stages released per commit
 #else
@@ -90,14 +101,17 @@ struct Plan {
   static constexpr int OFF_SA = OFF_ST + S * STAGE_BYTES;  // 2 x BT fp32 scales
   static constexpr int OFF_BAR = OFF_SA + 2 * BT * 4;
   static constexpr int NUM_BARS = 2 * S8 + S + S / REL + 2 + 2 + 2 + 1;
-  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + 1024;  // + align slack
+  static constexpr int ALIGN_SLACK = KS == 1 ? 1024 : 0;
+  static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + ALIGN_SLACK;
   static constexpr uint32_t TMEM_COLS = 2 * BT;  // two accumulators of BT fp32 columns
-  static_assert(OFF_ST % 1024 == 0 && W16_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0,
+  static_assert(OFF_ST % 1024 == 0 && W16_SUB % 1024 == 0 && X16_SUB % 1024 == 0 &&
+                    STAGE_BYTES % 1024 == 0,
                 "swizzled stages need 1 KB alignment");
   static_assert(S % REL == 0, "stages are released in groups of REL");
 };
-static_assert(Plan<true, 256>::SMEM_BYTES <= 232448, "shared memory plan too large");
-static_assert(Plan<false, 128>::SMEM_BYTES <= 232448, "shared memory plan too large");
+static_assert(Plan<true, 256, 1>::SMEM_BYTES <= 232448, "shared memory plan too large");
+static_assert(Plan<true, 256, 2>::SMEM_BYTES <= 232448, "shared memory plan too large");
+static_assert(Plan<false, 128, 1>::SMEM_BYTES <= 232448, "shared memory plan too large");
 
 // instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
 // M = 128 (weights), N = BT (tokens)
@@ -304,31 +318,32 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int j) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
 }
 
-// Converts `rows` rows x 64 codes of a staged tile into the swizzled fp16
-// operand tile.  Unit u = (row u / 4, codes 16 (u % 4) .. +16): one 16-byte
-// load (8 bytes of packed INT4) and two 16-byte stores into swizzled chunks
-// 2 (u % 4) and 2 (u % 4) + 1.  A warp covers 8 whole rows; each 8-thread
-// store phase writes two rows' even (or odd) chunks, which the 128-byte
-// swizzle puts in disjoint banks.  All of a thread's units (UPT of them) are
-// loaded before any is converted, so a tile costs one shared-memory round
-// trip per thread, not one per unit.
-template <bool INT4, int NT, int ROWS>
+// Converts ROWS rows x (64 KS) codes of a staged tile into KS swizzled fp16
+// operand sub-tiles (ROWS x 64 each, 128-byte rows, ROWS * 128 bytes apart).
+// Unit u = (row u / (4 KS), codes 16 (u % (4 KS)) .. +16): one 16-byte load
+// (8 bytes of packed INT4) and two 16-byte stores into the swizzled chunks
+// 2 c4 and 2 c4 + 1 of its sub-tile's row (c4 = unit % 4).  All of a
+// thread's units (UPT of them) are loaded before any is converted, so a
+// stage costs one shared-memory round trip per thread, not one per unit.
+template <bool INT4, int NT, int ROWS, int KS>
 __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, int ct) {
-  constexpr int units = ROWS * 4;
+  constexpr int UPR = 4 * KS;                  // units per row
+  constexpr int units = ROWS * UPR;
   constexpr int UPT = (units + NT - 1) / NT;  // units per thread
+  constexpr int SRC_ROW = INT4 ? 32 * KS : 64 * KS;
   uint4 v[UPT];
 #pragma unroll
   for (int i = 0; i < UPT; ++i) {
     const int u = ct + i * NT;
     v[i] = make_uint4(0, 0, 0, 0);
     if (u < units) {
-      const int r = u >> 2, c = u & 3;
+      const int r = u / UPR, c = u % UPR;
       if (INT4) {
-        const uint2 w = *reinterpret_cast<const uint2 *>(src + r * 32 + c * 8);
+        const uint2 w = *reinterpret_cast<const uint2 *>(src + r * SRC_ROW + c * 8);
         v[i].x = w.x;
         v[i].y = w.y;
       } else {
-        v[i] = *reinterpret_cast<const uint4 *>(src + r * 64 + c * 16);
+        v[i] = *reinterpret_cast<const uint4 *>(src + r * SRC_ROW + c * 16);
       }
     }
   }
@@ -336,7 +351,8 @@ __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, i
   for (int i = 0; i < UPT; ++i) {
     const int u = ct + i * NT;
     if (u < units) {
-      const int r = u >> 2, c = u & 3;
+      const int r = u / UPR, c = u % UPR;
+      const int sub = c >> 2, c4 = c & 3;
       uint4 lo, hi;
       if (INT4) {
         lo = i4x8_to_h(v[i].x);
@@ -345,10 +361,10 @@ __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, i
         lo = i8x8_to_h(make_uint2(v[i].x, v[i].y));
         hi = i8x8_to_h(make_uint2(v[i].z, v[i].w));
       }
-      uint8_t *row = dst + (r >> 3) * 1024 + (r & 7) * 128;
+      uint8_t *row = dst + sub * (ROWS * 128) + (r >> 3) * 1024 + (r & 7) * 128;
       const int x = r & 7;
-      *reinterpret_cast<uint4 *>(row + (((2 * c) ^ x) << 4)) = lo;
-      *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ x) << 4)) = hi;
+      *reinterpret_cast<uint4 *>(row + (((2 * c4) ^ x) << 4)) = lo;
+      *reinterpret_cast<uint4 *>(row + (((2 * c4 + 1) ^ x) << 4)) = hi;
     }
   }
 }
@@ -534,14 +550,19 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
 
 // ------------------------------------------------------------- kernel ----
 
-template <int WBITS, bool PERGROUP, bool XH, int BT>
+template <int WBITS, bool PERGROUP, bool XH, int BT, int KS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmW, const TcParams p) {
-  using PL = Plan<XH, BT>;
+  using PL = Plan<XH, BT, KS>;
   constexpr int S8 = PL::S8, S = PL::S;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
+  if (PL::ALIGN_SLACK == 0 && (raw & 1023u) != 0) {
+    // the plan has no slack for aligning by hand: report and do nothing
+    if (threadIdx.x == 0 && p.err != nullptr) atomicCAS(p.err, 0u, static_cast<unsigned>(kDevErrSmemAlign));
+    return;
+  }
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *sm = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -559,7 +580,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t drain_bar = bar0 + 8u * (B_ACC + 6);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + PL::OFF_BAR + PL::NUM_BARS * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  auto w16 = [&](int s) { return base + PL::OFF_ST + s * PL::STAGE_BYTES; };
+  auto w16 = [&](int s) { return base + PL::OFF_ST + s * PL::STAGE_BYTES; };  // + j W16_SUB
   auto x16 = [&](int s) { return base + PL::OFF_ST + s * PL::STAGE_BYTES + PL::W16_BYTES; };
 
   if (threadIdx.x == 0) {
@@ -625,9 +646,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             mbar_arrive_expect_tx(full8(s8), bytes8);
             tma_load_2d(base + PL::OFF_W8 + s8 * PL::W8_BYTES, &tmW, full8(s8),
-                        WBITS == 8 ? kb * BK : kb * (BK / 2), nb * BW);
+                        WBITS == 8 ? kb * PL::KB : kb * (PL::KB / 2), nb * BW);
             if (!XH)
-              tma_load_2d(base + PL::OFF_X8 + s8 * PL::X8_BYTES, &tmX, full8(s8), kb * BK, tb * BT);
+              tma_load_2d(base + PL::OFF_X8 + s8 * PL::X8_BYTES, &tmX, full8(s8), kb * PL::KB,
+                          tb * BT);
             pend |= 1u << s8;
             pph = (pph & ~(1u << s8)) | (ph8 << s8);
             if (++s8 == S8) {
@@ -654,7 +676,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             mbar_arrive_expect_tx(full(s), PL::X16_BYTES);
-            tma_load_2d(x16(s), &tmX, full(s), kb * BK, tb * BT);
+#pragma unroll
+            for (int j = 0; j < KS; ++j)
+              tma_load_2d(x16(s) + j * PL::X16_SUB, &tmX, full(s), kb * PL::KB + j * BK, tb * BT);
             pend |= 1u << s;
             pph = (pph & ~(1u << s)) | (ph << s);
             if (++s == S) {
@@ -691,9 +715,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t d = tmem + r * BT;
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              tc_mma(d, sw128_desc(w16(s) + k * 32), sw128_desc(x16(s) + k * 32), idesc<BT>(),
-                     (first && k == 0) ? 0u : 1u);
+            for (int j = 0; j < KS; ++j) {
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                tc_mma(d, sw128_desc(w16(s) + j * PL::W16_SUB + k * 32),
+                       sw128_desc(x16(s) + j * PL::X16_SUB + k * 32), idesc<BT>(),
+                       (first && j == 0 && k == 0) ? 0u : 1u);
+              }
             }
             if ((s % REL) == REL - 1) tc_commit(empty(s / REL));
             if ((kb % chunk_kb) == chunk_kb - 1 || kb == nkb - 1) {
@@ -727,11 +755,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          convert_tile<WBITS == 4, NT, BW>(sm + PL::OFF_W8 + s8 * PL::W8_BYTES,
-                                           sm + (w16(s) - base), ct);
+          convert_tile<WBITS == 4, NT, BW, KS>(sm + PL::OFF_W8 + s8 * PL::W8_BYTES,
+                                               sm + (w16(s) - base), ct);
           if (!XH)
-            convert_tile<false, NT, BT>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES,
-                                        sm + (x16(s) - base), ct);
+            convert_tile<false, NT, BT, KS>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES,
+                                            sm + (x16(s) - base), ct);
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
@@ -803,15 +831,15 @@ bool make_map(CUtensorMap *map, const void *ptr, long rows, long cols, int elem_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int WBITS, bool PERGROUP, bool XH, int BT>
+template <int WBITS, bool PERGROUP, bool XH, int BT, int KS>
 int launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, cudaStream_t s) {
   static bool attr_set[64] = {};
   static int sms[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return W8A8_ERR_CUDA;
-  constexpr int smem = Plan<XH, BT>::SMEM_BYTES;
+  constexpr int smem = Plan<XH, BT, KS>::SMEM_BYTES;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<WBITS, PERGROUP, XH, BT>,
+    if (cudaFuncSetAttribute(gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return W8A8_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -819,34 +847,36 @@ int launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, cu
     attr_set[dev] = true;
   }
   const int grid = p.ntiles < sms[dev] ? p.ntiles : sms[dev];
-  gemm_tc_kernel<WBITS, PERGROUP, XH, BT><<<grid, NUM_THREADS, smem, s>>>(tx, tw, p);
+  gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS><<<grid, NUM_THREADS, smem, s>>>(tx, tw, p);
   return launch_status();
 }
 
 template <bool XH, int BT>
 int launch_modes(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, int wbits,
                  cudaStream_t s) {
-  if (wbits == 4) return launch_t<4, false, XH, BT>(tx, tw, p, s);
-  if (p.gs != 0) return launch_t<8, true, XH, BT>(tx, tw, p, s);
-  return launch_t<8, false, XH, BT>(tx, tw, p, s);
+  if (wbits == 4) return launch_t<4, false, XH, BT, 1>(tx, tw, p, s);
+  if (p.gs != 0) return launch_t<8, true, XH, BT, 1>(tx, tw, p, s);
+  return launch_t<8, false, XH, BT, 1>(tx, tw, p, s);
 }
 
 }  // namespace
 
 // X (activations) is int8 codes [M, K] (x_half false) or the same codes as
 // fp16 values (x_half true).  256-token tiles for fp16 codes with M > 128,
-// else 128.
+// else 128; per channel, those 256-token tiles take two K blocks per stage.
 int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, const float *sw,
                    int M, int N, int K, int group_size, int wbits, __half *y,
                    int32_t *acc_out, cudaStream_t s) {
   // INT8 activation codes are converted in the kernel too: 128-token tiles
   const int bt = (M <= 128 || !x_half) ? 128 : 256;
+  const int ks = (bt == 256 && group_size == 0) ? 2 : 1;
+  const int kb = BK * ks;  // K per stage
   CUtensorMap tx, tw;
   if (!make_map(&tx, X, M, K, x_half ? 2 : 1, bt, BK)) return W8A8_ERR_CUDA;
   if (wbits == 8) {
-    if (!make_map(&tw, W, N, K, 1, BW, BK)) return W8A8_ERR_CUDA;
+    if (!make_map(&tw, W, N, K, 1, BW, kb)) return W8A8_ERR_CUDA;
   } else {
-    if (!make_map(&tw, W, N, K / 2, 1, BW, BK / 2)) return W8A8_ERR_CUDA;
+    if (!make_map(&tw, W, N, K / 2, 1, BW, kb / 2)) return W8A8_ERR_CUDA;
   }
   unsigned int *err = device_error_word();
   if (err == nullptr) return W8A8_ERR_CUDA;
@@ -856,12 +886,12 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
   p.K = K;
   p.gs = group_size;
   p.G = groups_of(K, group_size);
-  p.nkb = (K + BK - 1) / BK;
-  // K blocks per exact fp32 chunk (see the header comment)
+  p.nkb = (K + kb - 1) / kb;  // stages per tile
+  // stages per exact fp32 chunk (see the header comment)
   if (group_size != 0)
-    p.chunk_kb = group_size / BK;
+    p.chunk_kb = group_size / kb;
   else
-    p.chunk_kb = wbits == 8 ? 1024 / BK : 16384 / BK;
+    p.chunk_kb = wbits == 8 ? 1024 / kb : 16384 / kb;
   p.nblocks = (N + BW - 1) / BW;
   const long tblocks = (M + bt - 1) / bt;
   const long ntiles = static_cast<long>(p.nblocks) * tblocks;
@@ -872,9 +902,13 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
   p.y = y;
   p.acc_out = acc_out;
   p.err = err;
-  if (x_half)
-    return bt == 128 ? launch_modes<true, 128>(tx, tw, p, wbits, s)
-                     : launch_modes<true, 256>(tx, tw, p, wbits, s);
+  if (x_half) {
+    if (bt == 128) return launch_modes<true, 128>(tx, tw, p, wbits, s);
+    if (ks == 2)
+      return wbits == 4 ? launch_t<4, false, true, 256, 2>(tx, tw, p, s)
+                        : launch_t<8, false, true, 256, 2>(tx, tw, p, s);
+    return launch_t<8, true, true, 256, 1>(tx, tw, p, s);
+  }
   return launch_modes<false, 128>(tx, tw, p, wbits, s);
 }
 
