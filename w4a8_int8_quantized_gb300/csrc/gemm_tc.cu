@@ -363,8 +363,13 @@ __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, i
       }
       uint8_t *row = dst + sub * (ROWS * 128) + (r >> 3) * 1024 + (r & 7) * 128;
       const int x = r & 7;
-      *reinterpret_cast<uint4 *>(row + (((2 * c4) ^ x) << 4)) = lo;
-      *reinterpret_cast<uint4 *>(row + (((2 * c4 + 1) ^ x) << 4)) = hi;
+      // the 8 lanes of a store phase cover one row of both sub-tiles when
+      // KS = 2 (same bank groups, 16 KB apart): odd sub-tiles store their
+      // odd chunk first, so each store instruction meets disjoint banks
+      const bool odd = (sub & 1) != 0;
+      const int c_first = odd ? 2 * c4 + 1 : 2 * c4;
+      *reinterpret_cast<uint4 *>(row + ((c_first ^ x) << 4)) = odd ? hi : lo;
+      *reinterpret_cast<uint4 *>(row + (((c_first ^ 1) ^ x) << 4)) = odd ? lo : hi;
     }
   }
 }
