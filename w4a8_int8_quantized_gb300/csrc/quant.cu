@@ -31,8 +31,17 @@ namespace {
 
 enum OutMode { kOutInt8 = 0, kOutHalf = 1, kOutInt4 = 2 };
 
+// Resident CTAs per SM to aim for: the loads in flight (the only latency
+// hiding this one-pass kernel has) scale with it.  Five CTAs (<= 51
+// registers) measured best where each thread holds at most 4 vectors; more
+// vectors keep the register count they need.
+template <int V>
+constexpr int quant_min_blocks() {
+  return V <= 4 ? 5 : V <= 7 ? 3 : V <= 14 ? 2 : 1;
+}
+
 template <int V, int MODE>
-__global__ void __launch_bounds__(256) row_quant_kernel(
+__global__ void __launch_bounds__(256, quant_min_blocks<V>()) row_quant_kernel(
     const uint4 *__restrict__ x, long R, int K, int gs, int qmax, int T,
     void *__restrict__ out, float *__restrict__ scale) {
   __shared__ float red[8];
