@@ -313,6 +313,18 @@ __device__ __forceinline__ uint4 i4x8_to_h(uint32_t w) {
   return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
+// Two scale products s_i * w with one paired fp32 multiply (each half an
+// IEEE multiply rounded to nearest; nothing follows it that could fuse).
+__device__ __forceinline__ void mul2(float s0, float s1, float w, float &p0, float &p1) {
+  asm("{\n.reg .b64 a, b, c;\n"
+      "mov.b64 a, {%2, %3};\n"
+      "mov.b64 b, {%4, %4};\n"
+      "mul.rn.f32x2 c, a, b;\n"
+      "mov.b64 {%0, %1}, c;\n}\n"
+      : "=f"(p0), "=f"(p1)
+      : "f"(s0), "f"(s1), "f"(w));
+}
+
 // byte offset of 16-byte chunk j of row r in a 128-byte-swizzled tile
 __device__ __forceinline__ uint32_t sw128_off(int r, int j) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
@@ -462,14 +474,14 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
               for (int i4 = 0; i4 < 8; ++i4) {
                 const float4 s4 =
                     lds_f32x4(sas + (gb * BT + half * CPT + j * 32 + i4 * 4) * 4);
-                const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+                float sc[4];
+                mul2(s4.x, s4.y, sw_g, sc[0], sc[1]);  // (s_a * s_w) first, as in the dequant rule
+                mul2(s4.z, s4.w, sw_g, sc[2], sc[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                   const int idx = j * 32 + i4 * 4 + e;
-                  // (s_a * s_w) first, as in the dequant rule
-                  acc[idx] = __float_as_uint(
-                      __fadd_rn(__uint_as_float(acc[idx]),
-                                __fmul_rn(__uint_as_float(v[i4 * 4 + e]), __fmul_rn(sv[e], sw_g))));
+                  acc[idx] = __float_as_uint(__fadd_rn(
+                      __uint_as_float(acc[idx]), __fmul_rn(__uint_as_float(v[i4 * 4 + e]), sc[e])));
                   asm volatile("" : "+r"(acc[idx]));  // before the next scale load
                 }
               }
