@@ -111,6 +111,7 @@ struct Plan {
 };
 static_assert(Plan<true, 256, 1>::SMEM_BYTES <= 232448, "shared memory plan too large");
 static_assert(Plan<true, 256, 2>::SMEM_BYTES <= 232448, "shared memory plan too large");
+static_assert(Plan<true, 128, 2>::SMEM_BYTES <= 232448, "shared memory plan too large");
 static_assert(Plan<false, 128, 1>::SMEM_BYTES <= 232448, "shared memory plan too large");
 
 // instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major,
@@ -880,13 +881,13 @@ int launch_modes(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p
 
 // X (activations) is int8 codes [M, K] (x_half false) or the same codes as
 // fp16 values (x_half true).  256-token tiles for fp16 codes with M > 128,
-// else 128; per channel, those 256-token tiles take two K blocks per stage.
+// else 128; per channel with fp16 codes, a stage holds two K blocks.
 int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, const float *sw,
                    int M, int N, int K, int group_size, int wbits, __half *y,
                    int32_t *acc_out, cudaStream_t s) {
   // INT8 activation codes are converted in the kernel too: 128-token tiles
   const int bt = (M <= 128 || !x_half) ? 128 : 256;
-  const int ks = (bt == 256 && group_size == 0) ? 2 : 1;
+  const int ks = (x_half && group_size == 0) ? 2 : 1;
   const int kb = BK * ks;  // K per stage
   CUtensorMap tx, tw;
   if (!make_map(&tx, X, M, K, x_half ? 2 : 1, bt, BK)) return W8A8_ERR_CUDA;
@@ -920,10 +921,14 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
   p.acc_out = acc_out;
   p.err = err;
   if (x_half) {
-    if (bt == 128) return launch_modes<true, 128>(tx, tw, p, wbits, s);
-    if (ks == 2)
+    if (ks == 2) {
+      if (bt == 128)
+        return wbits == 4 ? launch_t<4, false, true, 128, 2>(tx, tw, p, s)
+                          : launch_t<8, false, true, 128, 2>(tx, tw, p, s);
       return wbits == 4 ? launch_t<4, false, true, 256, 2>(tx, tw, p, s)
                         : launch_t<8, false, true, 256, 2>(tx, tw, p, s);
+    }
+    if (bt == 128) return launch_t<8, true, true, 128, 1>(tx, tw, p, s);
     return launch_t<8, true, true, 256, 1>(tx, tw, p, s);
   }
   return launch_modes<false, 128>(tx, tw, p, wbits, s);
