@@ -69,9 +69,6 @@ constexpr int kCtasPerSm = 2;
 #else
 constexpr int kCtasPerSm = W8A8_MV_CTAS_PER_SM;
 #endif
-#ifndef W8A8_MV_NO_PDL
-#define W8A8_MV_NO_PDL 0
-#endif
 constexpr int kAccBytesMax = 32 * 1024;  // per-row (per-group) state per CTA
 constexpr int kRingBytes = kThreads * kD * kU * 16;  // per CTA
 
@@ -181,16 +178,12 @@ __global__ void __launch_bounds__(kThreads, 2 * kCtasPerSm) mv_kernel(
     cp_async_commit();
   };
 
-#if !W8A8_MV_NO_PDL
   asm volatile("griddepcontrol.launch_dependents;");
-#endif
   // ---- before the wait: reads of Wq only ----
 #pragma unroll
   for (int t = 0; t < kD; ++t) issue(t);
-#if !W8A8_MV_NO_PDL
   // everything below may read what the previous kernel on the stream wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
-#endif
 
   for (int i = tid; i < rows * G; i += kThreads) {
     acc[i] = 0;
@@ -391,7 +384,7 @@ int launch_mv(const void *xin, const float *sa, const void *W, const float *sw, 
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = W8A8_MV_NO_PDL ? 0 : 1;
+  cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, mv_kernel<WBITS, PERGROUP, FUSED>, xin, sa,
                          static_cast<const uint8_t *>(W), sw, N, K, gs, y) != cudaSuccess) {
     cudaGetLastError();
