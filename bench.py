@@ -295,6 +295,107 @@ def run_reference(args):
 
 # -------------------------------------------------------------- GPU path --
 
+def measure_workloads(w8, torch, device, flush_l2, l2_bytes, tflops_peak, hbm_peak, reps=10):
+    """Every other workload of the layer, timed once per case with CUDA events
+    (median of `reps`): the 512 x 512 per-channel layer, per group gs 128 /
+    64, W4A8 at M = 2048 and M = 1, and the linear layers of an 8B-class
+    decoder block at M = 4516 and M = 1.  GEMM-type calls run after an L2
+    flush; decode calls run back to back over weight copies larger than L2
+    (a decode step walks layer after layer).  Seeded synthetic inputs."""
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, per_rep_flush=True, inner=1):
+        ts = []
+        for _ in range(reps):
+            torch.cuda._sleep(int(2e6))  # the host enqueues the rep while the GPU waits
+            if per_rep_flush:
+                flush_l2()
+            e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            e0.record(stream)
+            for i in range(inner):
+                fn(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / inner)
+        return statistics.median(ts)
+
+    def dev(a):
+        return torch.from_numpy(a).to(device)
+
+    out = {}
+
+    def gemm_case(name, M, N, K, gs, wbits, act):
+        x = dev(synth.activations(M, K, seed=0, **act))
+        W = dev(synth.weights(N, K, seed=0))
+        wq, sw = (w8.quantize_weight_int8(W, gs) if wbits == 8 else w8.pack_weight_int4(W))
+        del W
+        xq, sa = w8.quantize_act_per_token_h(x, gs)
+        y = torch.empty((M, N), dtype=torch.float16, device=device)
+        for _ in range(2):
+            w8.quantize_act_per_token_h(x, gs, xq, sa)
+            w8.w8a8_gemm_h(xq, sa, wq, sw, gs, wbits, y)
+        q_ms = timed(lambda i: w8.quantize_act_per_token_h(x, gs, xq, sa))
+        g_ms = timed(lambda i: w8.w8a8_gemm_h(xq, sa, wq, sw, gs, wbits, y))
+        tops = 2.0 * M * N * K / (g_ms * 1e-3) / 1e12
+        out[name] = {"M": M, "N": N, "K": K, "group_size": gs, "wbits": wbits,
+                     "quant_ms": round(q_ms, 5), "gemm_ms": round(g_ms, 5),
+                     "gemm_TOPS": round(tops, 1), "gemm_frac_of_peak": round(tops / tflops_peak, 4)}
+        return g_ms + q_ms
+
+    def decode_case(name, layers, wbits, act):
+        """layers: [(N, K)]; one decode step = linear() on every layer in turn."""
+        sets = []
+        per_set = sum(n * (k if wbits == 8 else k // 2) for n, k in layers)
+        copies = max(2, int(3 * l2_bytes // per_set) + 1)
+        xs = [dev(synth.activations(1, k, seed=0, **act)) for _, k in layers]
+        ys = [torch.empty((1, n), dtype=torch.float16, device=device) for n, _ in layers]
+        base = []
+        for n, k in layers:
+            W = dev(synth.weights(n, k, seed=0))
+            base.append(w8.quantize_weight_int8(W) if wbits == 8 else w8.pack_weight_int4(W))
+            del W
+        for c in range(copies):
+            sets.append([(wq.clone(), sw) for wq, sw in base] if c else base)
+        ws = [torch.empty(max(w8.w8a8_linear_workspace_bytes(1, k), 1), dtype=torch.uint8,
+                          device=device) for _, k in layers]
+
+        def step(i):
+            for li, (wq, sw) in enumerate(sets[i % copies]):
+                w8.linear(xs[li], wq, sw, 0, wbits, workspace=ws[li], y=ys[li])
+        for i in range(copies):
+            step(i)
+        us = timed(step, per_rep_flush=False, inner=copies) * 1e3
+        nbytes = sum(n * (k if wbits == 8 else k // 2) + 4 * n + 2 * k + 2 * n for n, k in layers)
+        out[name] = {"layers": [list(l) for l in layers], "wbits": wbits, "weight_copies": copies,
+                     "us_per_step": round(us, 3), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac_of_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+        del sets
+
+    wl = synth.WORKLOADS
+    # the 512 x 512 per-channel layer: the whole linear() call
+    small = wl["pc_small"]
+    x = dev(synth.activations(128, 512, seed=0, **small["act"]))
+    wq, sw = w8.quantize_weight_int8(dev(synth.weights(512, 512, seed=0)))
+    y = torch.empty((128, 512), dtype=torch.float16, device=device)
+    ws0 = torch.empty(w8.w8a8_linear_workspace_bytes(128, 512), dtype=torch.uint8, device=device)
+    w8.linear(x, wq, sw, workspace=ws0, y=y)
+    out["pc_small_M128_N512_K512"] = {"linear_ms": round(timed(
+        lambda i: w8.linear(x, wq, sw, workspace=ws0, y=y)), 5)}
+    for gs in wl["pg"]["gs"]:
+        gemm_case(f"per_group_gs{gs}_M4096", 4096, 10240, 2560, gs, 8, wl["pg"]["act"])
+    gemm_case("w4a8_M2048", 2048, 14336, 4096, 0, 4, wl["w4a8"]["act"])
+    decode_case("w4a8_M1_decode", [(14336, 4096)], 4, wl["w4a8"]["act"])
+    total = 0.0
+    for lname, n, k in synth.BLOCK_LAYERS:
+        total += gemm_case(f"block_{lname}_M4516", 4516, n, k, 0, 8, synth.BLOCK_ACT)
+    ops = sum(2.0 * 4516 * n * k for _, n, k in synth.BLOCK_LAYERS)
+    out["block_prefill_M4516_total"] = {"ms": round(total, 5),
+                                         "TOPS": round(ops / (total * 1e-3) / 1e12, 1)}
+    decode_case("block_decode_M1_step", [(n, k) for _, n, k in synth.BLOCK_LAYERS], 8,
+                synth.BLOCK_ACT)
+    return out
+
+
 def run_ours(args):
     import ctypes
 
@@ -520,6 +621,11 @@ def run_ours(args):
             "gpu_launches": args.steps * (2 * len(MS) - 1),  # M=1 is one fused launch
             "clocks": clocks.summary(), "decode": decode, "detail": detail,
             "wall_s_timed_region": round(wall, 4)}
+    if rank == 0 and not args.no_workloads:
+        hbm = _peak(peaks, "hbm_gbs") if peak_src == "measured" else None
+        line["workloads"] = measure_workloads(
+            w8, torch, device, flush_l2, l2, peak,
+            hbm if hbm is not None else FALLBACK_PEAKS["hbm_gbs"])
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inputs)
     if rank == 0:
@@ -586,6 +692,8 @@ def main():
                     help="skip the timed CPU-oracle sample (about 15 s)")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the back-to-back decode measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the timing of the other workloads (per group, W4A8, decoder block)")
     ap.add_argument("--only", choices=["quant", "quant_i8", "gemm", "gemm_i8", "w4a8", "linear",
                                        "linear4"],
                     help="run one kernel of the path on one shape (for profilers)")
