@@ -78,8 +78,11 @@ int w8a8_is_available(void);
 const char *w8a8_status_string(int status);
 
 /* Reads and clears the device-side error word that the kernels set when a
- * bounded wait on the tensor-core pipeline gives up.  Synchronizes `stream`.
- * Returns W8A8_OK, W8A8_ERR_TIMEOUT or W8A8_ERR_CUDA. */
+ * bounded wait on the tensor-core pipeline gives up, or when a GEMM kernel
+ * finds its shared memory not 1 KB aligned and returns without doing
+ * anything (both leave the outputs of that call undefined).  Synchronizes
+ * `stream`.  Returns W8A8_OK, W8A8_ERR_TIMEOUT (for either cause) or
+ * W8A8_ERR_CUDA. */
 int w8a8_check_status(w8a8_stream_t stream);
 
 /* Offline INT8 weight quantization ("cider 설치와 사용법":

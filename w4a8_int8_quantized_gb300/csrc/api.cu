@@ -116,7 +116,7 @@ const char *w8a8_status_string(int status) {
     case W8A8_ERR_MISALIGNED: return "misaligned pointer or K";
     case W8A8_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
     case W8A8_ERR_CUDA: return "CUDA error";
-    case W8A8_ERR_TIMEOUT: return "device-side wait timed out";
+    case W8A8_ERR_TIMEOUT: return "device-side wait timed out (or kernel did not run: shared memory misaligned)";
     case W8A8_ERR_WORKSPACE: return "workspace too small or misaligned";
     default: return "unknown status";
   }
