@@ -26,7 +26,8 @@
 // 128-row one.  The activations arrive either as fp16 codes, which TMA
 // places directly in the MMA's layout, or as INT8 codes, converted too.
 //
-// Kernel layout (persistent, one CTA of 16 warps per SM, 64-deep K blocks):
+// Kernel layout (persistent, one CTA of 16 warps per SM; a pipeline stage
+// holds KS 64-deep K blocks, KS = 2 per channel with fp16 codes, else 1):
 //   warp 0      TMA producer: INT8 / packed INT4 weight tiles into a staging
 //               ring; activation tiles into the staging ring (INT8) or
 //               straight into the MMA operand stage (fp16 codes, 128-byte
