@@ -101,7 +101,7 @@ struct Plan {
   static constexpr int OFF_ST = OFF_X8 + S8 * X8_BYTES;    // stage s: W16, then X16
   static constexpr int OFF_SA = OFF_ST + S * STAGE_BYTES;  // 2 x BT fp32 scales
   static constexpr int OFF_BAR = OFF_SA + 2 * BT * 4;
-  static constexpr int NUM_BARS = 2 * S8 + S + S / REL + 2 + 2 + 2 + 1;
+  static constexpr int NUM_BARS = 2 * S8 + S * KS + S / REL + 2 + 2 + 2 + 1;  // full: one per sub-tile
   static constexpr int ALIGN_SLACK = KS == 1 ? 1024 : 0;
   static constexpr int SMEM_BYTES = OFF_BAR + NUM_BARS * 8 + 16 + ALIGN_SLACK;
   static constexpr uint32_t TMEM_COLS = 2 * BT;  // two accumulators of BT fp32 columns
@@ -332,17 +332,19 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int j) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
 }
 
-// Converts ROWS rows x (64 KS) codes of a staged tile into KS swizzled fp16
-// operand sub-tiles (ROWS x 64 each, 128-byte rows, ROWS * 128 bytes apart).
-// Unit u = (row u / (4 KS), codes 16 (u % (4 KS)) .. +16): one 16-byte load
-// (8 bytes of packed INT4) and two 16-byte stores into the swizzled chunks
-// 2 c4 and 2 c4 + 1 of its sub-tile's row (c4 = unit % 4).  All of a
-// thread's units (UPT of them) are loaded before any is converted, so a
-// stage costs one shared-memory round trip per thread, not one per unit.
+// Converts sub-tile `sub` (codes 64 sub .. 64 sub + 63 of each of ROWS rows)
+// of a staged tile of ROWS x (64 KS) codes into its swizzled fp16 operand
+// sub-tile (ROWS x 64, 128-byte rows; sub-tiles ROWS * 128 bytes apart).
+// Unit u = (row u / 4, codes 16 (u % 4) .. +16 of the sub-tile): one 16-byte
+// load (8 bytes of packed INT4) and two 16-byte stores into the swizzled
+// chunks 2 (u % 4) and 2 (u % 4) + 1 of its row.  A warp covers 8 whole
+// rows; each 8-thread store phase writes two rows' even (or odd) chunks,
+// which the 128-byte swizzle puts in disjoint banks.  All of a thread's
+// units (UPT of them) are loaded before any is converted, so a sub-tile
+// costs one shared-memory round trip per thread, not one per unit.
 template <bool INT4, int NT, int ROWS, int KS>
-__device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, int ct) {
-  constexpr int UPR = 4 * KS;                  // units per row
-  constexpr int units = ROWS * UPR;
+__device__ __forceinline__ void convert_sub(const uint8_t *src, uint8_t *dst, int ct, int sub) {
+  constexpr int units = ROWS * 4;
   constexpr int UPT = (units + NT - 1) / NT;  // units per thread
   constexpr int SRC_ROW = INT4 ? 32 * KS : 64 * KS;
   uint4 v[UPT];
@@ -351,7 +353,7 @@ __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, i
     const int u = ct + i * NT;
     v[i] = make_uint4(0, 0, 0, 0);
     if (u < units) {
-      const int r = u / UPR, c = u % UPR;
+      const int r = u >> 2, c = sub * 4 + (u & 3);
       if (INT4) {
         const uint2 w = *reinterpret_cast<const uint2 *>(src + r * SRC_ROW + c * 8);
         v[i].x = w.x;
@@ -365,8 +367,7 @@ __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, i
   for (int i = 0; i < UPT; ++i) {
     const int u = ct + i * NT;
     if (u < units) {
-      const int r = u / UPR, c = u % UPR;
-      const int sub = c >> 2, c4 = c & 3;
+      const int r = u >> 2, c4 = u & 3;
       uint4 lo, hi;
       if (INT4) {
         lo = i4x8_to_h(v[i].x);
@@ -377,13 +378,8 @@ __device__ __forceinline__ void convert_tile(const uint8_t *src, uint8_t *dst, i
       }
       uint8_t *row = dst + sub * (ROWS * 128) + (r >> 3) * 1024 + (r & 7) * 128;
       const int x = r & 7;
-      // the 8 lanes of a store phase cover one row of both sub-tiles when
-      // KS = 2 (same bank groups, 16 KB apart): odd sub-tiles store their
-      // odd chunk first, so each store instruction meets disjoint banks
-      const bool odd = (sub & 1) != 0;
-      const int c_first = odd ? 2 * c4 + 1 : 2 * c4;
-      *reinterpret_cast<uint4 *>(row + ((c_first ^ x) << 4)) = odd ? hi : lo;
-      *reinterpret_cast<uint4 *>(row + (((c_first ^ 1) ^ x) << 4)) = odd ? lo : hi;
+      *reinterpret_cast<uint4 *>(row + (((2 * c4) ^ x) << 4)) = lo;
+      *reinterpret_cast<uint4 *>(row + (((2 * c4 + 1) ^ x) << 4)) = hi;
     }
   }
 }
@@ -589,10 +585,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t bar0 = base + PL::OFF_BAR;
   auto full8 = [&](int s) { return bar0 + 8u * s; };
   auto empty8 = [&](int s) { return bar0 + 8u * (S8 + s); };
-  auto full = [&](int s) { return bar0 + 8u * (2 * S8 + s); };
+  // full(s, j): sub-tile j of stage s is in place (its converters and its
+  // activation copy), so the MMAs of a stage start on its first sub-tile
+  auto full = [&](int s, int j) { return bar0 + 8u * (2 * S8 + s * KS + j); };
   constexpr int REL = PL::REL;
-  auto empty = [&](int g) { return bar0 + 8u * (2 * S8 + S + g); };  // per release group
-  constexpr int B_ACC = 2 * S8 + S + S / REL;
+  auto empty = [&](int g) { return bar0 + 8u * (2 * S8 + S * KS + g); };  // per release group
+  constexpr int B_ACC = 2 * S8 + S * KS + S / REL;
   auto accfull = [&](int r) { return bar0 + 8u * (B_ACC + r); };
   auto accempty = [&](int r) { return bar0 + 8u * (B_ACC + 2 + r); };
   auto saready = [&](int b) { return bar0 + 8u * (B_ACC + 4 + b); };
@@ -607,7 +605,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(full8(s), 1);
       mbar_init(empty8(s), PL::CONV_WARPS);
     }
-    for (int s = 0; s < S; ++s) mbar_init(full(s), PL::CONV_WARPS + (XH ? 1 : 0));
+    for (int s = 0; s < S; ++s)
+      for (int j = 0; j < KS; ++j) mbar_init(full(s, j), PL::CONV_WARPS + (XH ? 1 : 0));
     for (int g = 0; g < S / REL; ++g) mbar_init(empty(g), 1);
     for (int r = 0; r < 2; ++r) {
       mbar_init(accfull(r), 1);
@@ -694,10 +693,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full(s), PL::X16_BYTES);
 #pragma unroll
-            for (int j = 0; j < KS; ++j)
-              tma_load_2d(x16(s) + j * PL::X16_SUB, &tmX, full(s), kb * PL::KB + j * BK, tb * BT);
+            for (int j = 0; j < KS; ++j) {
+              mbar_arrive_expect_tx(full(s, j), PL::X16_SUB);
+              tma_load_2d(x16(s) + j * PL::X16_SUB, &tmX, full(s, j), kb * PL::KB + j * BK,
+                          tb * BT);
+            }
             pend |= 1u << s;
             pph = (pph & ~(1u << s)) | (ph << s);
             if (++s == S) {
@@ -707,7 +708,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         for (int i = 0; i < S; ++i)
-          if ((pend >> i) & 1u) wait_bar_teardown(full(i), (pph >> i) & 1u);
+          if ((pend >> i) & 1u)
+            for (int j = 0; j < KS; ++j) wait_bar_teardown(full(i, j), (pph >> i) & 1u);
       }
     } else if (warp == 1) {
       // ---------------------------------------------------- MMA issuer ----
@@ -727,14 +729,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               tc_fence_after();
             }
-            if (!wait_bar(full(s), ph, abort_flag, kDevErrFullBarrier, p.err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
             const uint32_t d = tmem + r * BT;
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
+              if (!wait_bar(full(s, j), ph, abort_flag, kDevErrFullBarrier, p.err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k) {
                 tc_mma(d, sw128_desc(w16(s) + j * PL::W16_SUB + k * 32),
@@ -742,6 +744,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        (first && j == 0 && k == 0) ? 0u : 1u);
               }
             }
+            if (!ok) break;
             if ((s % REL) == REL - 1) tc_commit(empty(s / REL));
             if ((kb % chunk_kb) == chunk_kb - 1 || kb == nkb - 1) {
               tc_commit(accfull(r));
@@ -774,17 +777,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          convert_tile<WBITS == 4, NT, BW, KS>(sm + PL::OFF_W8 + s8 * PL::W8_BYTES,
-                                               sm + (w16(s) - base), ct);
-          if (!XH)
-            convert_tile<false, NT, BT, KS>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES,
-                                            sm + (x16(s) - base), ct);
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(full(s));
-            mbar_arrive(empty8(s8));
+#pragma unroll
+          for (int j = 0; j < KS; ++j) {
+            convert_sub<WBITS == 4, NT, BW, KS>(sm + PL::OFF_W8 + s8 * PL::W8_BYTES,
+                                                sm + (w16(s) - base), ct, j);
+            if (!XH)
+              convert_sub<false, NT, BT, KS>(sm + PL::OFF_X8 + s8 * PL::X8_BYTES,
+                                             sm + (x16(s) - base), ct, j);
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full(s, j));
           }
+          if (lane == 0) mbar_arrive(empty8(s8));
           if (++s8 == S8) {
             s8 = 0;
             ph8 ^= 1u;
