@@ -327,11 +327,6 @@ __device__ __forceinline__ void mul2(float s0, float s1, float w, float &p0, flo
       : "f"(s0), "f"(s1), "f"(w));
 }
 
-// byte offset of 16-byte chunk j of row r in a 128-byte-swizzled tile
-__device__ __forceinline__ uint32_t sw128_off(int r, int j) {
-  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
-}
-
 // Converts sub-tile `sub` (codes 64 sub .. 64 sub + 63 of each of ROWS rows)
 // of a staged tile of ROWS x (64 KS) codes into its swizzled fp16 operand
 // sub-tile (ROWS x 64, 128-byte rows; sub-tiles ROWS * 128 bytes apart).
