@@ -154,7 +154,11 @@ int w4a8_gemm(const int8_t *xq, const float *scale_a, const uint8_t *Wp,
  * tensor-core GEMM reads without converting, which linear() uses for M > 1.
  *   x        fp16 [M, K]
  *   xq_h     fp16 [M, K]        (out) the codes q, as fp16
- *   scale_a  fp32 [M, G]        (out) */
+ *   scale_a  fp32 [M, G]        (out)
+ * Ordering: the kernel lets the next kernel on the stream start early
+ * (griddepcontrol.launch_dependents), which only matters to a kernel
+ * launched with programmatic stream serialization; the library's GEMM is,
+ * and it waits for this kernel to finish before reading any input. */
 int quantize_act_per_token_h(const w8a8_half *x, int M, int K, int group_size,
                              w8a8_half *xq_h, float *scale_a, w8a8_stream_t stream);
 
@@ -163,7 +167,10 @@ int quantize_act_per_token_h(const w8a8_half *x, int M, int K, int group_size,
  * writes them.  Codes outside [-127, 127] or not integral are outside the
  * contract.  Always the tensor-core GEMM, for any M >= 1.
  *   xq_h fp16 [M, K], scale_a fp32 [M, G]; Wq int8 [N, K] or packed uint8
- *   [N, K/2]; scale_w fp32 [N, G]; y fp16 [M, N] (out) */
+ *   [N, K/2]; scale_w fp32 [N, G]; y fp16 [M, N] (out)
+ * The GEMM (any M, every GEMM entry point) is launched with programmatic
+ * stream serialization: its set-up may overlap the previous kernel on the
+ * stream, and it reads no input before that kernel has finished. */
 int w8a8_gemm_h(const w8a8_half *xq_h, const float *scale_a, const void *Wq,
                 const float *scale_w, int M, int N, int K, int group_size, int wbits,
                 w8a8_half *y, w8a8_stream_t stream);

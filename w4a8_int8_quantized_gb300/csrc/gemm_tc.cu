@@ -42,6 +42,9 @@
 //               one output channel and BT / 2 tokens, so a warp's store
 //               writes 32 consecutive channels of one token.  The
 //               activation scales of the tile are staged in shared memory.
+// The kernel is launched as a programmatic dependent of the previous one on
+// the stream: its set-up (barriers, TMEM) may overlap that kernel's tail,
+// and griddepcontrol.wait precedes every read of an input.
 // Stages hand over through mbarriers; every wait is bounded, and a wait that
 // gives up records a code in the device error word, raises an abort flag
 // seen by every role, lets in-flight copies and MMAs land, frees TMEM and
@@ -626,6 +629,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a programmatic dependent: the set-up above may overlap the
+  // previous kernel on the stream; every read of an input comes after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int nkb = p.nkb, chunk_kb = p.chunk_kb;
 
@@ -865,7 +871,21 @@ int launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, cu
     attr_set[dev] = true;
   }
   const int grid = p.ntiles < sms[dev] ? p.ntiles : sms[dev];
-  gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS><<<grid, NUM_THREADS, smem, s>>>(tx, tw, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS>, tx, tw, p) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return W8A8_ERR_CUDA;
+  }
   return launch_status();
 }
 

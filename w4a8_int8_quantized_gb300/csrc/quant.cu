@@ -44,6 +44,10 @@ template <int V, int MODE>
 __global__ void __launch_bounds__(256, quant_min_blocks<V>()) row_quant_kernel(
     const uint4 *__restrict__ x, long R, int K, int gs, int qmax, int T,
     void *__restrict__ out, float *__restrict__ scale) {
+  // activation codes for the GEMM: let it launch now and run its prologue
+  // while this grid finishes (it waits for this grid before reading any
+  // input); the weight quantizers (other modes) never start dependents early
+  if (MODE == kOutHalf) asm volatile("griddepcontrol.launch_dependents;");
   __shared__ float red[8];
   const int nvec = K >> 3;
   const int t = threadIdx.x % T;
