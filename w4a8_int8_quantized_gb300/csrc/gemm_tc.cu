@@ -36,7 +36,9 @@
 //               128 x BT x 16 tcgen05.mma per K block into one of two TMEM
 //               accumulators (ping-pong per chunk);
 //   warps 2-7   converters: INT8 / INT4 codes -> fp16, written in the
-//               128-byte-swizzled K-major layout the MMA reads;
+//               128-byte-swizzled K-major layout the MMA reads, one K block
+//               of a stage at a time, each announced on its own barrier so
+//               that the MMAs start on a stage's first block;
 //   warps 8-15  epilogue: drain TMEM (tcgen05.ld), exact int32 sums or fp32
 //               per-group rescale, then the fp16 output; each thread owns
 //               one output channel and BT / 2 tokens, so a warp's store
