@@ -17,7 +17,8 @@ value    = sum over the sweep of 2*M*N*K integer ops / device time of the step
            the two kernels.
 e2e      = the same metric through the C ABI's ``linear`` call with pinned
            host buffers: host->device copy of x, the layer, device->host copy
-           of y, all inside the timed events.
+           of y, all inside the timed events; from M = 2048 on, in chunks of
+           1024 rows whose copies and layer calls overlap on three streams.
 roofline = the dominant kernel (the GEMM at M=8192): 2*M*N*K / its average
            CUDA-event duration in the breakdown pass, against the measured
            dense fp16/bf16 tensor peak; traffic = DRAM bytes per launch from
@@ -59,6 +60,7 @@ UNIT = "TOPS"
 # section "cider의 성능 측정 결과"): the same metric as a whole-sweep rate.
 PAGES_MS = {1: 0.27, 128: 0.34, 1024: 1.23, 4096: 4.41, 8192: 8.71}
 PAGES_TOPS = sum(2.0 * m * N_OUT * K_IN for m in MS) / (sum(PAGES_MS.values()) * 1e-3) / 1e12
+E2E_CHUNK_ROWS = 1024  # rows per pipelined chunk of the e2e measurement
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -497,16 +499,61 @@ def run_ours(args):
         if record is not None:
             record.append(evs)
 
-    def e2e_step(record):
-        evs = []
-        for m in MS:
-            b = bufs[m]
-            flush_l2()
-            e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
-            e0.record(stream)
+    # e2e: from M = 2048 on, the rows go in chunks of E2E_CHUNK_ROWS, the
+    # host->device copy of chunk i+1, the layer on chunk i and the
+    # device->host copy of chunk i-1 overlapping on three streams (the copy
+    # engines of the two directions and the SMs work at once); smaller M runs
+    # copy, layer, copy in order (there the host enqueues more slowly than
+    # the GPU would run chunks)
+    s_h2d, s_comp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    comp_ptr = ctypes.c_void_p(s_comp.cuda_stream)
+
+    def e2e_chunks(m):
+        return m // E2E_CHUNK_ROWS if m >= 2 * E2E_CHUNK_ROWS else 1
+
+    def linear_rows(m, r0, r1, sptr):
+        b = bufs[m]
+        x, y = b["x"][r0:r1], b["y"][r0:r1]
+        check(lib.linear(P(x.data_ptr()), P(wq.data_ptr()), P(sw.data_ptr()), r1 - r0, N_OUT,
+                         K_IN, 0, 8, P(b["ws"].data_ptr()), b["ws"].numel(), P(y.data_ptr()),
+                         sptr), "linear")
+
+    def e2e_call(m, e0):
+        b = bufs[m]
+        C = e2e_chunks(m)
+        if C == 1:
             b["x"].copy_(b["xh"], non_blocking=True)
             call_linear(m, b["x"], b["y"])
             b["yh"].copy_(b["y"], non_blocking=True)
+            return
+        for st in (s_h2d, s_comp, s_d2h):
+            st.wait_event(e0)
+        ends = []
+        for i in range(C):
+            r0, r1 = m * i // C, m * (i + 1) // C
+            with torch.cuda.stream(s_h2d):
+                b["x"][r0:r1].copy_(b["xh"][r0:r1], non_blocking=True)
+                eh = torch.cuda.Event()
+                eh.record(s_h2d)
+            s_comp.wait_event(eh)
+            linear_rows(m, r0, r1, comp_ptr)
+            ec = torch.cuda.Event()
+            ec.record(s_comp)
+            s_d2h.wait_event(ec)
+            with torch.cuda.stream(s_d2h):
+                b["yh"][r0:r1].copy_(b["y"][r0:r1], non_blocking=True)
+        for st in (s_h2d, s_comp, s_d2h):
+            ev = torch.cuda.Event()
+            ev.record(st)
+            stream.wait_event(ev)
+
+    def e2e_step(record):
+        evs = []
+        for m in MS:
+            flush_l2()
+            e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            e0.record(stream)
+            e2e_call(m, e0)
             e1.record(stream)
             evs.append((m, e0, e1))
         if record is not None:
@@ -642,7 +689,11 @@ def run_ours(args):
             "data": "synthetic", "config": config_dict(), "roofline": roofline,
             "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
                     "h2d_bytes_per_step": sum(m * K_IN * 2 for m in MS),
-                    "d2h_bytes_per_step": sum(m * N_OUT * 2 for m in MS)},
+                    "d2h_bytes_per_step": sum(m * N_OUT * 2 for m in MS),
+                    "method": f"C ABI linear() per M from pinned host buffers, L2 flushed "
+                              f"before each M; M >= {2 * E2E_CHUNK_ROWS} in chunks of "
+                              f"{E2E_CHUNK_ROWS} rows with copy-in, layer and copy-out "
+                              f"overlapped on three streams"},
             "gpu_launches": args.steps * (2 * len(MS) - 1),  # M=1 is one fused launch
             "clocks": clocks.summary(), "decode": decode, "detail": detail,
             "wall_s_timed_region": round(wall, 4)}
