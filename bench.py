@@ -613,6 +613,16 @@ def run_ours(args):
     e2e_ms = sum(e0.elapsed_time(e1) for evs in rec2 for _, e0, e1 in evs) / args.steps
     e2e_ms = max_over_ranks(e2e_ms, ws, device)
     e2e_value = ws * step_ops() / (e2e_ms * 1e-3) / 1e12
+    # the outputs the chunked three-stream path copied back must equal one
+    # linear() call over all rows on one stream (bit for bit: the rows of a
+    # chunk are computed exactly as in the whole call)
+    e2e_mismatch = 0
+    for m in MS:
+        b = bufs[m]
+        y_ref = torch.empty_like(b["y"])
+        call_linear(m, b["x"], y_ref)
+        torch.cuda.synchronize()
+        e2e_mismatch += int((y_ref.cpu().view(torch.int16) != b["yh"].view(torch.int16)).sum())
 
     # decode, back to back over distinct weight copies
     decode = None
@@ -693,7 +703,9 @@ def run_ours(args):
                     "method": f"C ABI linear() per M from pinned host buffers, L2 flushed "
                               f"before each M; M >= {2 * E2E_CHUNK_ROWS} in chunks of "
                               f"{E2E_CHUNK_ROWS} rows with copy-in, layer and copy-out "
-                              f"overlapped on three streams"},
+                              f"overlapped on three streams",
+                    "outputs_equal_single_stream_linear": e2e_mismatch == 0,
+                    "mismatched_outputs": e2e_mismatch},
             "gpu_launches": args.steps * (2 * len(MS) - 1),  # M=1 is one fused launch
             "clocks": clocks.summary(), "decode": decode, "detail": detail,
             "wall_s_timed_region": round(wall, 4)}

@@ -27,6 +27,11 @@
  *  - Every pointer is a DEVICE pointer on the current CUDA device, owned by
  *    the caller.  The library allocates no device memory and keeps no
  *    pointer after a call returns.
+ *  - The library caches per-device state (function attributes, the SM
+ *    count, the device addresses of its own device variables) on the first
+ *    call on each device; the caches are thread-safe.  Do not use the
+ *    library on a device after cudaDeviceReset() in the same process: the
+ *    cached addresses would be stale.
  *  - Matrix pointers (x, W, Wq, Wp, xq, y, acc, workspace) must be 16-byte
  *    aligned, scale pointers 4-byte aligned, and K a multiple of 16 (32 for
  *    packed INT4 weights), else W8A8_ERR_MISALIGNED.  K is at most 32768
@@ -224,6 +229,19 @@ int linear_noalloc(const w8a8_half *x, const void *Wq, const float *scale_w, int
 int w8a8_gemm_i32(const int8_t *xq, const void *Wq, int M, int N, int K,
                   int group_size, int wbits, int32_t *acc,
                   w8a8_stream_t stream);
+
+/* Test hook of the failure path (the method has no counterpart): sets, for
+ * the tensor-core GEMM launches that follow (every entry point that runs
+ * it), the limit of its bounded device-side waits in SM clock cycles
+ * (0 = the default, about 2 s) and, with skip_first_copy = 1, leaves the
+ * first weight-staging copy of each CTA unissued, so that the wait for it
+ * gives up: the kernel then returns early, its outputs are undefined, and
+ * w8a8_check_status() reports W8A8_ERR_TIMEOUT.  No fault, trap or hang is
+ * involved; the kernel still lets every copy it issued land before it
+ * exits.  Process-wide; w8a8_test_set_fault(0, 0) restores normal
+ * operation.  Returns W8A8_ERR_INVALID_ARG for a negative limit or a flag
+ * other than 0 / 1. */
+int w8a8_test_set_fault(long long wait_limit_cycles, int skip_first_copy);
 
 #ifdef __cplusplus
 }

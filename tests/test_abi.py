@@ -4,6 +4,8 @@ reported before any device work; the workspace size rule."""
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -104,3 +106,34 @@ def test_binding_raises_without_touching_device():
         binding.quantize_act_per_token(torch.zeros(4, 64, dtype=torch.float32))
     with pytest.raises(ValueError):
         binding.quantize_act_per_token(torch.zeros(4, 64, dtype=torch.float16))  # CPU tensor
+
+
+NO_DEVICE_SCRIPT = r"""
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+from w4a8_int8_quantized_gb300 import binding
+lib = binding.load()
+P = ctypes.c_void_p
+assert lib.w8a8_is_available() == 0
+# aligned fake addresses: the device check refuses before any launch
+assert lib.quantize_act_per_token(P(1 << 20), 4, 64, 0, P(2 << 20), P(3 << 20), P(0)) == 3
+assert lib.w8a8_gemm(P(1 << 20), P(3 << 20), P(2 << 20), P(3 << 20), 4, 8, 64, 0, P(4 << 20),
+                     P(0)) == 3
+assert lib.linear_noalloc(P(1 << 20), P(2 << 20), P(3 << 20), 4, 8, 64, 0, 8, P(4 << 20),
+                          P(0)) == 3
+assert lib.w8a8_test_set_fault(-1, 0) == 1 and lib.w8a8_test_set_fault(0, 2) == 1
+assert lib.w8a8_test_set_fault(0, 0) == 0
+print("no-device ok")
+"""
+
+
+def test_no_visible_device_is_unsupported(lib):
+    """With no CUDA device visible (CUDA_VISIBLE_DEVICES empty), the library
+    still loads, w8a8_is_available() is 0 and every compute call returns
+    W8A8_ERR_UNSUPPORTED_DEVICE after its host checks, launching nothing (the
+    analogue of the SDK's is_available() gate, "cider 설치와 사용법")."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", NO_DEVICE_SCRIPT, ROOT], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "no-device ok" in r.stdout

@@ -190,6 +190,125 @@ def test_int32_worst_case_magnitudes():
     assert host(acc).max() == 127 * 127 * K
 
 
+# ---------------------------------- exactness of the fp32 tensor-core sums ----
+#
+# The contraction runs on kind::f16 tensor cores with an fp32 accumulator
+# that is drained every K-chunk (1024 for INT8 weights, 16384 for INT4).  It
+# is exact only if the accumulator keeps every bit of an integer below 2^24
+# while each 16-deep MMA adds an integer of any parity.  These inputs drive
+# the running sum of every chunk of every (token, channel) pair into
+# [2^23, 2^24), with per-MMA increments of random parity and runs of +-1
+# products added to an accumulator already near 2^24; a tensor core that
+# aligned its addends with fewer than 24 significant bits would lose low
+# bits here.
+
+CHUNK = {8: 1024, 4: 16384}
+
+
+def _large_partial_operands(M, N, K, wbits, seed):
+    """a [M, K], w [N, K] with a[m, k] w[n, k] >= 0 almost everywhere: a is
+    +-127 with one sign pattern s(k) shared by all rows, w is s(k) times a
+    magnitude drawn from the top of the range; every chunk then sums to
+    between 2^23 and 2^24.  Row variants: a tail of each chunk with +-1
+    activations (small increments on a large accumulator), weights whose
+    chunk tails are +-1, a few perturbed activations, and all-negative
+    products (negative accumulators)."""
+    rng = np.random.default_rng(seed)
+    qmax = 127 if wbits == 8 else 7
+    lo = 100 if wbits == 8 else 5
+    chunk = CHUNK[wbits]
+    s = np.where(rng.random(K) < 0.5, -1, 1).astype(np.int64)
+    kin = np.arange(K) % chunk
+    a = np.tile(127 * s, (M, 1))
+    for m in range(M):
+        kind = m % 4
+        if kind == 1:      # the last 1/8 of every chunk: +-1 activations
+            tail = kin >= chunk - chunk // 8
+            a[m, tail] = s[tail]
+        elif kind == 2:    # a few perturbed magnitudes (odd and even)
+            idx = rng.choice(K, size=min(K, 40), replace=False)
+            a[m, idx] = s[idx] * rng.integers(1, 128, size=idx.size)
+        elif kind == 3:    # negative products: the accumulator runs to -2^24
+            a[m] = -a[m]
+    w = s * rng.integers(lo, qmax + 1, size=(N, K))
+    for n in range(0, N, 3):  # every third channel: +-1 weights at chunk tails
+        tail = kin >= chunk - chunk // 16
+        w[n, tail] = s[tail]
+    return a.astype(np.int8), w.astype(np.int8)
+
+
+def _chunk_partials(a, w, chunk):
+    """Exact running partial of every chunk at its end, [M, N, K / chunk]."""
+    a64, w64 = a.astype(np.int64), w.astype(np.int64)
+    K = a.shape[1]
+    return np.stack([a64[:, c:c + chunk] @ w64[:, c:c + chunk].T for c in range(0, K, chunk)],
+                    axis=-1)
+
+
+@pytest.mark.parametrize("M,N,K,wbits", [(130, 257, 4096, 8), (257, 130, 2048, 8),
+                                         (130, 96, 32768, 4), (3, 33, 16384, 4)])
+def test_int32_sums_exact_at_large_partials(M, N, K, wbits):
+    a, w = _large_partial_operands(M, N, K, wbits, seed=K + M)
+    part = np.abs(_chunk_partials(a, w, CHUNK[wbits]))
+    # the inputs do what they are for: most chunk partials in [2^23, 2^24)
+    assert part.max() < 2 ** 24
+    assert np.mean(part >= 2 ** 23) > 0.5
+    wdev = dev(w) if wbits == 8 else dev(oracle.pack_int4(w))
+    acc = w8.w8a8_gemm_i32(dev(a), wdev, 0, wbits)
+    np.testing.assert_array_equal(host(acc), oracle.int_gemm(a, w))
+
+
+def _cancelling_operands(M, N, wbits, seed):
+    """K = two chunks; the second chunk holds the products of the first with
+    the opposite sign, in a different order along K, plus a few activations
+    one or two below full scale.  Each chunk partial is near 2^24 while the
+    exact total is small (|total| < 2048), so the fp16 output y = total (unit
+    scales) shows any bit a chunk lost."""
+    rng = np.random.default_rng(seed)
+    chunk = CHUNK[wbits]
+    qmax = 127 if wbits == 8 else 7
+    lo = 100 if wbits == 8 else 5
+    s = np.where(rng.random(chunk) < 0.5, -1, 1).astype(np.int64)
+    v = rng.integers(lo, qmax + 1, size=(N, chunk))
+    perm = rng.permutation(chunk)
+    a1 = 127 * s
+    a = np.empty((M, 2 * chunk), np.int64)
+    a[:, :chunk] = a1
+    a[:, chunk + perm] = a1
+    w = np.empty((N, 2 * chunk), np.int64)
+    w[:, :chunk] = s * v
+    w[:, chunk + perm] = -(s * v)
+    for m in range(M):  # perturb a few activations: total = -sum d * v
+        half = m % 2
+        idx = rng.choice(chunk, size=rng.integers(0, 8), replace=False)
+        d = rng.integers(1, 3, size=idx.size)
+        cols = idx if half == 0 else chunk + perm[idx]
+        a[m, cols] = (127 - d) * s[idx]
+    return a.astype(np.int8), w.astype(np.int8)
+
+
+@pytest.mark.parametrize("M,N,wbits", [(130, 257, 8), (300, 129, 8), (130, 64, 4)])
+def test_fp16_output_exact_at_large_partials(M, N, wbits):
+    """Through the layer's own GEMM (fp16 codes, w8a8_gemm_h): with unit
+    scales the fp16 output is the exact integer total, which stays below
+    2048 although every chunk partial is near 2^24."""
+    a, w = _cancelling_operands(M, N, wbits, seed=M + N)
+    K = a.shape[1]
+    part = np.abs(_chunk_partials(a, w, CHUNK[wbits]))
+    assert part.min() >= 2 ** 22 and part.max() < 2 ** 24
+    ref_acc = oracle.int_gemm(a, w)
+    assert np.abs(ref_acc).max() < 2048
+    sa = np.ones((M, 1), np.float32)
+    sw = np.ones((N, 1), np.float32)
+    ref = oracle.dequant(ref_acc, sa, sw)
+    wdev = dev(w) if wbits == 8 else dev(oracle.pack_int4(w))
+    y = host(w8.w8a8_gemm_h(dev(a.astype(np.float16)), dev(sa), wdev, dev(sw), 0, wbits))
+    assert_bits(y, ref)
+    acc = host(w8.w8a8_gemm_i32(dev(a), wdev, 0, wbits))
+    np.testing.assert_array_equal(acc, ref_acc)
+    assert K == 2 * CHUNK[wbits]
+
+
 # ------------------------------------------------------ fused dequant ----
 
 GEMM_CASES = [(130, 257, 512, 0), (257, 130, 2560, 0), (64, 96, 4096, 64),
@@ -332,4 +451,32 @@ def test_outputs_outside_the_problem_are_untouched():
 
 
 def test_device_status_clean_after_calls():
+    assert w8.w8a8_check_status() == 0
+
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """Failure detection without a fault: with the test hook, every CTA of
+    the GEMM leaves its first weight-staging copy unissued and the role waits
+    are limited to ~1 ms, so the converters' wait for that stage runs out.
+    The kernel must return (abort flag, in-flight copies and MMAs allowed to
+    land, TMEM freed), w8a8_check_status must report W8A8_ERR_TIMEOUT, and
+    the context must stay usable: the next call is exact and the status
+    clean."""
+    M, N, K = 130, 257, 512
+    rng = np.random.default_rng(5)
+    a = rng.integers(-127, 128, size=(M, K), dtype=np.int8)
+    w = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    ref = oracle.int_gemm(a, w)
+    ad, wd = dev(a), dev(w)
+    assert w8.w8a8_check_status() == 0
+    try:
+        w8.w8a8_test_set_fault(2_000_000, True)
+        w8.w8a8_gemm_i32(ad, wd)
+        status = w8.w8a8_check_status()
+    finally:
+        w8.w8a8_test_set_fault(0, False)
+    assert status == 5, w8.w8a8_status_string(status)
+    assert w8.w8a8_check_status() == 0  # read-and-clear
+    acc = w8.w8a8_gemm_i32(ad, wd)
+    np.testing.assert_array_equal(host(acc), ref)
     assert w8.w8a8_check_status() == 0

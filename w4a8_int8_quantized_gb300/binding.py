@@ -29,7 +29,8 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "misaligned pointer or K",
 EXPORTS = ("w8a8_is_available", "w8a8_status_string", "w8a8_check_status",
            "quantize_weight_int8", "pack_weight_int4", "quantize_act_per_token",
            "w8a8_gemm", "w8a8_mv", "w4a8_gemm", "quantize_act_per_token_h", "w8a8_gemm_h",
-           "w8a8_linear_workspace_bytes", "linear", "linear_noalloc", "w8a8_gemm_i32")
+           "w8a8_linear_workspace_bytes", "linear", "linear_noalloc", "w8a8_gemm_i32",
+           "w8a8_test_set_fault")
 
 
 class W8A8Error(RuntimeError):
@@ -66,6 +67,7 @@ def load(path: str | None = None):
             "linear": ([P, P, P, I, I, I, I, I, P, Z, P, P], I),
             "linear_noalloc": ([P, P, P, I, I, I, I, I, P, P], I),
             "w8a8_gemm_i32": ([P, P, I, I, I, I, I, P, P], I),
+            "w8a8_test_set_fault": ([ctypes.c_longlong, I], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -295,3 +297,11 @@ def w8a8_gemm_i32(xq, Wq, group_size: int = 0, wbits: int = 8, acc=None):
     _check(load().w8a8_gemm_i32(_ptr(xq), _ptr(Wq), M, N, K, group_size, wbits, _ptr(acc),
                                 _stream()), "w8a8_gemm_i32")
     return acc
+
+
+def w8a8_test_set_fault(wait_limit_cycles: int = 0, skip_first_copy: bool = False) -> None:
+    """Test hook: the GEMM's bounded-wait limit (cycles, 0 = default) and
+    whether its first weight-staging copy per CTA is left unissued, for the
+    launches that follow."""
+    _check(load().w8a8_test_set_fault(int(wait_limit_cycles), int(bool(skip_first_copy))),
+           "w8a8_test_set_fault")

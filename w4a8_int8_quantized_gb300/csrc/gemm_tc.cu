@@ -53,6 +53,9 @@
 // returns.
 #include <cuda.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace w8a8 {
@@ -61,7 +64,10 @@ namespace {
 constexpr int BW = 128, BK = 64;  // weight rows (output channels) per tile, K block
 constexpr int NUM_THREADS = 512;
 constexpr int EPI_WARPS = 8, EPI_THREADS = EPI_WARPS * 32;
-constexpr long long kTimeoutCycles = 4000000000LL;  // about 2 s at 2 GHz
+// Limit of every bounded wait, in SM clock cycles (about 2 s at 2 GHz).  The
+// role waits take theirs from the launch (TcParams::wait_limit, this value
+// unless a test shortened it); the teardown waits always use this one.
+constexpr long long kTimeoutCycles = 4000000000LL;
 
 // Shared-memory plan.  XH: activations arrive as fp16 codes (TMA straight
 // into the operand layout); BT: tokens per tile (activations as INT8 codes
@@ -135,6 +141,8 @@ struct TcParams {
   __half *y;
   int32_t *acc_out;
   unsigned int *err;
+  long long wait_limit;  // role waits give up after this many cycles
+  int skip_first_copy;   // test only: leave the first staging copy of each CTA unissued
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -258,7 +266,7 @@ __device__ __forceinline__ void stg_b32(void *ptr, int v) {
 // (then it records `code` and raises the abort flag).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
                                          volatile int *abort_flag, unsigned int code,
-                                         unsigned int *err) {
+                                         unsigned int *err, long long limit) {
 #pragma unroll 1
   for (int i = 0; i < 32; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -266,7 +274,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       if (err != nullptr) atomicCAS(err, 0u, code);
       *abort_flag = 1;
       return false;
@@ -453,9 +461,9 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
           mbar_arrive(saready(gb));
           if (n < p.N) sw_g = __ldg(p.sw + n * p.G + c);
         }
-        bool w = wait_bar(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err);
+        bool w = wait_bar(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
         if (PERGROUP && want_y)
-          w = w && wait_bar(saready(gb), gph, abort_flag, kDevErrAccumBarrier, p.err);
+          w = w && wait_bar(saready(gb), gph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
@@ -525,7 +533,7 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
         continue;
       }
       if (!PERGROUP) {
-        bool w = wait_bar(saready(sb), sph, abort_flag, kDevErrAccumBarrier, p.err);
+        bool w = wait_bar(saready(sb), sph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
         if (!__all_sync(0xffffffffu, w)) break;
       }
       if (n >= p.N) continue;
@@ -661,18 +669,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
           const int nb = tile % p.nblocks, tb = tile / p.nblocks;
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bar(empty8(s8), ph8 ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
+            if (!wait_bar(empty8(s8), ph8 ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full8(s8), bytes8);
-            tma_load_2d(base + PL::OFF_W8 + s8 * PL::W8_BYTES, &tmW, full8(s8),
-                        WBITS == 8 ? kb * PL::KB : kb * (PL::KB / 2), nb * BW);
-            if (!XH)
-              tma_load_2d(base + PL::OFF_X8 + s8 * PL::X8_BYTES, &tmX, full8(s8), kb * PL::KB,
-                          tb * BT);
-            pend |= 1u << s8;
-            pph = (pph & ~(1u << s8)) | (ph8 << s8);
+            // (test only) a stage left unissued: its full barrier never
+            // completes, so the converters' bounded wait on it runs out
+            if (!(p.skip_first_copy && tile == static_cast<int>(blockIdx.x) && kb == 0)) {
+              mbar_arrive_expect_tx(full8(s8), bytes8);
+              tma_load_2d(base + PL::OFF_W8 + s8 * PL::W8_BYTES, &tmW, full8(s8),
+                          WBITS == 8 ? kb * PL::KB : kb * (PL::KB / 2), nb * BW);
+              if (!XH)
+                tma_load_2d(base + PL::OFF_X8 + s8 * PL::X8_BYTES, &tmX, full8(s8),
+                            kb * PL::KB, tb * BT);
+              pend |= 1u << s8;
+              pph = (pph & ~(1u << s8)) | (ph8 << s8);
+            }
             if (++s8 == S8) {
               s8 = 0;
               ph8 ^= 1u;
@@ -692,7 +704,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kb = 0; kb < nkb; ++kb) {
             // a release group is refilled once the MMAs of its last use are done
             if ((s % REL) == 0 &&
-                !wait_bar(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err)) {
+                !wait_bar(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit)) {
               ok = false;
               break;
             }
@@ -726,7 +738,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t r = cc & 1u;
             if (first) {
               if (!wait_bar(accempty(r), ((cc >> 1) & 1u) ^ 1u, abort_flag, kDevErrTmemEmpty,
-                            p.err)) {
+                            p.err, p.wait_limit)) {
                 ok = false;
                 break;
               }
@@ -735,7 +747,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t d = tmem + r * BT;
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
-              if (!wait_bar(full(s, j), ph, abort_flag, kDevErrFullBarrier, p.err)) {
+              if (!wait_bar(full(s, j), ph, abort_flag, kDevErrFullBarrier, p.err, p.wait_limit)) {
                 ok = false;
                 break;
               }
@@ -773,9 +785,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb) {
-          bool w = wait_bar(full8(s8), ph8, abort_flag, kDevErrFullBarrier, p.err);
+          bool w = wait_bar(full8(s8), ph8, abort_flag, kDevErrFullBarrier, p.err, p.wait_limit);
           if ((s % REL) == 0)
-            w = w && wait_bar(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err);
+            w = w && wait_bar(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit);
           if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
@@ -824,6 +836,8 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
   if (fn == nullptr) {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -837,6 +851,10 @@ EncodeTiledFn encode_fn() {
   }
   return fn;
 }
+
+// Role-wait limit and test switch for the next launches (w8a8_test_set_fault).
+std::atomic<long long> g_wait_limit{kTimeoutCycles};
+std::atomic<int> g_skip_first_copy{0};
 
 // 2-D tensor map over a row-major [rows, cols] matrix of 1- or 2-byte
 // elements, box [box_rows, box_cols]; out-of-range elements read 0.  2-byte
@@ -859,20 +877,27 @@ bool make_map(CUtensorMap *map, const void *ptr, long rows, long cols, int elem_
 
 template <int WBITS, bool PERGROUP, bool XH, int BT, int KS>
 int launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, cudaStream_t s) {
+  // per device: the shared-memory attribute set once, and the SM count
   static bool attr_set[64] = {};
   static int sms[64] = {};
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return W8A8_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W8A8_ERR_CUDA;
   constexpr int smem = Plan<XH, BT, KS>::SMEM_BYTES;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return W8A8_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return W8A8_ERR_CUDA;
-    attr_set[dev] = true;
+  int nsm = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return W8A8_ERR_CUDA;
+      if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return W8A8_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+    nsm = sms[dev];
   }
-  const int grid = p.ntiles < sms[dev] ? p.ntiles : sms[dev];
+  const int grid = p.ntiles < nsm ? p.ntiles : nsm;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(NUM_THREADS);
@@ -942,6 +967,8 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
   p.y = y;
   p.acc_out = acc_out;
   p.err = err;
+  p.wait_limit = g_wait_limit.load();
+  p.skip_first_copy = g_skip_first_copy.load();
   if (x_half) {
     if (ks == 2) {
       if (bt == 128)
@@ -957,3 +984,11 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
 }
 
 }  // namespace w8a8
+
+extern "C" int w8a8_test_set_fault(long long wait_limit_cycles, int skip_first_copy) {
+  if (wait_limit_cycles < 0 || (skip_first_copy != 0 && skip_first_copy != 1))
+    return W8A8_ERR_INVALID_ARG;
+  w8a8::g_wait_limit.store(wait_limit_cycles == 0 ? w8a8::kTimeoutCycles : wait_limit_cycles);
+  w8a8::g_skip_first_copy.store(skip_first_copy);
+  return W8A8_OK;
+}

@@ -46,6 +46,8 @@
 //    written by a kernel that lets this one start early (one that executes
 //    griddepcontrol.launch_dependents); the library's kernels that write
 //    weights do not.
+#include <mutex>
+
 #include "common.cuh"
 #include "quant_rule.cuh"
 
@@ -348,26 +350,33 @@ __global__ void __launch_bounds__(kThreads, 2 * kCtasPerSm) mv_kernel(
 template <int WBITS, bool PERGROUP, bool FUSED>
 int launch_mv(const void *xin, const float *sa, const void *W, const float *sw, int N, int K,
               int gs, __half *y, cudaStream_t s) {
+  // per device: the shared-memory attribute set once, and the SM count
   static bool attr_set[64] = {};
   static int sms[64] = {};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W8A8_ERR_CUDA;
   const int G = PERGROUP ? K / gs : 1;
   const int per_row = G * 4 * (PERGROUP ? 2 : 1);  // shared bytes per weight row
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(mv_kernel<WBITS, PERGROUP, FUSED>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kRingBytes + kMaxK + 4 * (kMaxK / 64) + kAccBytesMax) !=
-        cudaSuccess)
-      return W8A8_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return W8A8_ERR_CUDA;
-    attr_set[dev] = true;
+  int nsm = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(mv_kernel<WBITS, PERGROUP, FUSED>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kRingBytes + kMaxK + 4 * (kMaxK / 64) + kAccBytesMax) !=
+          cudaSuccess)
+        return W8A8_ERR_CUDA;
+      if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return W8A8_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+    nsm = sms[dev];
   }
   // kCtasPerSm CTAs per SM, more when a CTA's rows would not fit its shared
   // state (at most kAccBytesMax bytes, i.e. at most 8192 rows)
   const long rows_cap = kAccBytesMax / per_row;
-  long grid = static_cast<long>(kCtasPerSm) * sms[dev];
+  long grid = static_cast<long>(kCtasPerSm) * nsm;
   const long need = (N + rows_cap - 1) / rows_cap;
   if (grid < need) grid = need;
   if (grid > N) grid = N;

@@ -1,6 +1,8 @@
 // Device-side error word shared by the kernels that contain bounded waits.
 // A kernel whose wait gives up stores a nonzero code (which wait) here and
 // returns; w8a8_check_status() reads and clears it.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace w8a8 {
@@ -10,8 +12,13 @@ __device__ unsigned int g_device_error = 0;
 
 unsigned int *device_error_word() {
   static unsigned int *cache[64] = {};
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
   if (cache[dev] == nullptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
