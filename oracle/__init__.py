@@ -63,9 +63,10 @@ def _load():
         lib.oracle_dequant.argtypes = [P, P, P, L, L, L, P]
         lib.oracle_sampled_outputs.argtypes = [P, P, P, P, L, L, L, L, P, P, L, P, P]
         lib.oracle_set_threads.argtypes = [I]
+        lib.oracle_weight_only.argtypes = [P, P, P, L, L, L, L, P]
         for f in (lib.oracle_quant_rows, lib.oracle_pack_int4, lib.oracle_unpack_int4,
                   lib.oracle_int_gemm, lib.oracle_dequant, lib.oracle_sampled_outputs,
-                  lib.oracle_num_threads):
+                  lib.oracle_num_threads, lib.oracle_weight_only):
             f.restype = ctypes.c_int
         lib.oracle_set_threads.restype = None
         _lib = lib
@@ -174,6 +175,23 @@ def sampled_outputs(a, sa, w, sw, rows, cols, group_size: int = 0):
     return acc, y
 
 
+def weight_only(x: np.ndarray, q: np.ndarray, sw: np.ndarray, group_size: int = 0) -> np.ndarray:
+    """Weight-only product y = x . (q * s_w)^T rounded once to fp16: fp16 x
+    [M, K], integer weight codes q int8 [N, K] (INT8, or INT4 unpacked),
+    s_w [N, G]."""
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    M, K = x.shape
+    N = q.shape[0]
+    assert q.shape[1] == K
+    G = 1 if group_size == 0 else K // group_size
+    sw = np.ascontiguousarray(sw, dtype=np.float32).reshape(N, G)
+    y = np.empty((M, N), dtype=np.float16)
+    _check(_load().oracle_weight_only(_ptr(x.view(np.uint16)), _ptr(q), _ptr(sw), M, N, K,
+                                      group_size, _ptr(y.view(np.uint16))), "weight_only")
+    return y
+
+
 # ---- composites: the whole layer, step by step -----------------------------
 
 def quantize_weight_int8(W: np.ndarray, group_size: int = 0):
@@ -202,3 +220,13 @@ def linear(x: np.ndarray, wq: np.ndarray, sw: np.ndarray, group_size: int = 0,
     K = x.shape[1]
     w = unpack_int4(wq, K) if wbits == 4 else wq
     return dequant(int_gemm(xq, w, group_size), sa, sw)
+
+
+def linear_weight_only(x: np.ndarray, wq: np.ndarray, sw: np.ndarray, group_size: int = 0,
+                       wbits: int = 8) -> np.ndarray:
+    """The W8A16 / W4A16 layer: fp16 x times the dequantized weights; wq is
+    int8 [N, K] (wbits 8, per channel or per group) or packed uint8 [N, K/2]
+    (wbits 4, per channel)."""
+    K = x.shape[1]
+    w = unpack_int4(wq, K) if wbits == 4 else wq
+    return weight_only(x, w, sw, group_size)

@@ -250,3 +250,43 @@ int oracle_sampled_outputs(const int8_t *a, const float *sa, const int8_t *w,
     }
     return status;
 }
+
+/* Weight-only product, the W8A16 / W4A16 baselines the method is measured
+ * against: fp16 activations times the weights dequantized from their integer
+ * codes, What[n, k] = q[n, k] * s_w[n, g(k)].  [P1] section on MLX's
+ * weight-only quantization (the weights are dequantized to fp16 on the fly
+ * and multiplied with fp16 activations); [P2] mode table (W8A16 / W4A16:
+ * fp16 activations, MLX's GEMM) and the latency table's w8a16 / w4a16
+ * columns.
+ * Reading: the result is the real product y = x . What^T, rounded once to
+ * fp16.  It is evaluated in double: every x * q product is exact, the group
+ * sums carry a relative error below 2^-40 at K <= 32768, and the last step
+ * rounds double -> fp16 directly.
+ *   y[m, n] = half( sum over g of s_w[n, g] * (sum over k in g of x[m, k] * q[n, k]) )
+ * x: fp16 bits [M, K]; q: int8 codes [N, K]; s_w: fp32 [N, G]; y: fp16 [M, N]. */
+int oracle_weight_only(const uint16_t *x, const int8_t *q, const float *sw, long M,
+                       long N, long K, long group_size, uint16_t *y) {
+    if (!x || !q || !sw || !y || M < 0 || N < 0 || K <= 0) return ORACLE_BAD_ARG;
+    long gs = group_size == 0 ? K : group_size;
+    if (gs <= 0 || K % gs != 0) return ORACLE_BAD_ARG;
+    long G = K / gs;
+    int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < M; ++m) {
+        for (long n = 0; n < N; ++n) {
+            double total = 0.0;
+            for (long g = 0; g < G; ++g) {
+                double part = 0.0;
+                for (long k = g * gs; k < (g + 1) * gs; ++k) {
+                    double xv = (double)half_to_float(x[m * K + k]);
+                    if (!isfinite(xv)) status = ORACLE_NONFINITE;
+                    part += xv * (double)q[n * K + k];
+                }
+                total += (double)sw[n * G + g] * part;
+            }
+            _Float16 h = (_Float16)total;
+            memcpy(&y[m * N + n], &h, sizeof h);
+        }
+    }
+    return status;
+}

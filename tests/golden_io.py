@@ -68,3 +68,25 @@ def linear_cases():
         elif key == "acc":
             cur[key] = _matrix(val, np.int64)
     return cases
+
+
+def weight_only_cases():
+    """Cases of weight_only_small.txt: each ends with its `y` line."""
+    cases, cur = [], None
+    for line in _lines("weight_only_small.txt"):
+        key, val = [p.strip() for p in line.split(":", 1)]
+        if key == "test":
+            cur = dict(name=val)
+        elif key == "gs":
+            cur["gs"] = int(val)
+        elif key == "x":
+            cur["x"] = _matrix(val, np.float16)
+        elif key == "q":
+            cur["q"] = _matrix(val, np.int8)
+        elif key == "sw":
+            cur["sw"] = _matrix(val, np.float32)
+        elif key == "y":
+            cur["y"] = _matrix(val, np.float16)
+            cases.append(cur)
+            cur = None
+    return cases

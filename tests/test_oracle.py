@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle
-from golden_io import act_quant_cases, int4_cases, linear_cases
+from golden_io import act_quant_cases, int4_cases, linear_cases, weight_only_cases
 from w4a8_int8_quantized_gb300 import synth
 
 
@@ -287,3 +287,106 @@ def test_w4a8_linear_equals_unpacked_w8_path():
     q4 = oracle.unpack_int4(p, 128)
     np.testing.assert_array_equal(oracle.linear(x, p, s4, 0, wbits=4),
                                   oracle.linear(x, q4, s4, 0, wbits=8))
+
+
+# ------------------------------------------ weight-only (W8A16 / W4A16) ----
+#
+# The baseline the method is measured against: fp16 activations times the
+# integer weights dequantized with their scales ("Apple Silicon의 AI 한계치는
+# …", the section on MLX's weight-only quantization; "cider 소개", mode table
+# and the w8a16 / w4a16 latency columns).
+
+@pytest.mark.parametrize("case", weight_only_cases(), ids=lambda c: c["name"])
+def test_golden_weight_only(case):
+    y = oracle.weight_only(case["x"], case["q"], case["sw"], case["gs"])
+    np.testing.assert_array_equal(y.view(np.uint16), case["y"].view(np.uint16))
+
+
+def test_weight_only_unit_rows_pick_one_weight():
+    """x = e_k (one 1 per row) selects column k: y[m, n] = fp16(q[n, k] * s_w[n, g(k)]),
+    rounded by numpy's own float64 -> float16 conversion."""
+    rng = np.random.default_rng(11)
+    K, N = 256, 37
+    q = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    for gs in (0, 64, 128):
+        G = 1 if gs == 0 else K // gs
+        sw = (rng.random((N, G)) * 0.05).astype(np.float32)
+        ks = rng.choice(K, size=20, replace=False)
+        x = np.zeros((ks.size, K), np.float16)
+        x[np.arange(ks.size), ks] = 1
+        y = oracle.weight_only(x, q, sw, gs)
+        g = ks // (K if gs == 0 else gs)
+        want = (q[:, ks].T.astype(np.float64) * sw[:, g].T.astype(np.float64)).astype(np.float16)
+        np.testing.assert_array_equal(y.view(np.uint16), want.view(np.uint16))
+
+
+def test_weight_only_matches_float64_matmul():
+    """Against numpy's float64 matmul of x with the dequantized weights (a
+    different summation order): within one fp16 ulp everywhere, and bit-equal
+    except where the exact value sits within 2^-35 (relative) of a rounding
+    boundary."""
+    rng = np.random.default_rng(12)
+    M, N, K = 33, 65, 512
+    x = synth.activations(M, K, seed=3, n_outliers=3, outlier_scale=30.0)
+    for gs, wbits in ((0, 8), (64, 8), (128, 8), (0, 4)):
+        W = synth.weights(N, K, seed=4 + gs)
+        if wbits == 8:
+            q, sw = oracle.quantize_weight_int8(W, gs)
+        else:
+            p, sw = oracle.pack_weight_int4(W)
+            q = oracle.unpack_int4(p, K)
+        G = sw.shape[1]
+        deq = q.astype(np.float64) * np.repeat(sw.astype(np.float64), K // G, axis=1)
+        ref64 = x.astype(np.float64) @ deq.T
+        ref = ref64.astype(np.float16)
+        y = oracle.weight_only(x, q, sw, gs)
+        ulp = np.spacing(np.abs(ref)).astype(np.float64)
+        assert np.all(np.abs(y.astype(np.float64) - ref.astype(np.float64)) <= ulp)
+        assert np.mean(y.view(np.uint16) == ref.view(np.uint16)) > 0.999
+        if wbits == 4:
+            np.testing.assert_array_equal(
+                oracle.linear_weight_only(x, p, sw, 0, 4).view(np.uint16), y.view(np.uint16))
+
+
+def test_weight_only_quantization_error_bound():
+    """|y - x . W^T| <= sum_k |x_k| s_w / 2 + half an fp16 ulp of y: the only
+    errors are the weight rounding (at most half a step each) and the final
+    fp16 rounding (per channel, INT8 and INT4)."""
+    M, N, K = 17, 40, 1024
+    x = synth.activations(M, K, seed=5, n_outliers=4, outlier_scale=40.0)
+    W = synth.weights(N, K, seed=6)
+    exact = x.astype(np.float64) @ W.astype(np.float64).T
+    xs = np.abs(x.astype(np.float64)).sum(axis=1)
+    for wbits in (8, 4):
+        if wbits == 8:
+            q, sw = oracle.quantize_weight_int8(W)
+            y = oracle.weight_only(x, q, sw)
+        else:
+            p, sw = oracle.pack_weight_int4(W)
+            y = oracle.linear_weight_only(x, p, sw, 0, 4)
+        bound = xs[:, None] * sw[:, 0][None, :].astype(np.float64) / 2 * (1 + 1e-6)
+        bound += np.spacing(np.abs(y)).astype(np.float64) / 2
+        assert np.all(np.abs(y.astype(np.float64) - exact) <= bound)
+
+
+def test_weight_only_special_cases():
+    """gs = K equals per channel; x -> -x gives y -> -y; integer x with
+    power-of-two scales equals the exact W8A8 path (s_a = 1, every step
+    exact); zero weights give zero."""
+    rng = np.random.default_rng(13)
+    M, N, K = 9, 21, 256
+    x = synth.activations(M, K, seed=7)
+    q = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    sw = (rng.random((N, 1)) * 0.05).astype(np.float32)
+    a = oracle.weight_only(x, q, sw, 0)
+    b = oracle.weight_only(x, q, sw, K)
+    np.testing.assert_array_equal(a.view(np.uint16), b.view(np.uint16))
+    np.testing.assert_array_equal((-a).view(np.uint16), oracle.weight_only(-x, q, sw).view(np.uint16))
+    xi = rng.integers(-127, 128, size=(M, K)).astype(np.float16)
+    xi[:, 0] = 127  # row absmax 127: the activation scale is exactly 1
+    sp = (2.0 ** -rng.integers(6, 12, size=(N, 1))).astype(np.float32)
+    xq, sa = oracle.quantize_act_per_token(xi)
+    assert np.all(sa == 1) and np.array_equal(xq, xi.astype(np.int8))
+    w8a8 = oracle.dequant(oracle.int_gemm(xq, q), sa, sp)
+    np.testing.assert_array_equal(oracle.weight_only(xi, q, sp).view(np.uint16), w8a8.view(np.uint16))
+    assert np.all(oracle.weight_only(x, np.zeros_like(q), sw) == 0)
