@@ -377,7 +377,38 @@ def measure_workloads(w8, torch, device, flush_l2, l2_bytes, tflops_peak, hbm_pe
                      "frac_of_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 4)}
         del sets
 
+    def few_rows_case():
+        """M = 2..32 rows of the N=10240, K=2560 layer: linear() (the few-row
+        kernel up to 16 rows, the GEMM above) against the quantizer + the
+        tensor-core GEMM on the same rows; each call after an L2 flush."""
+        sweep = wl["pc_sweep"]
+        W = dev(synth.weights(sweep["N"], sweep["K"], seed=0))
+        wq, sw = w8.quantize_weight_int8(W)
+        del W
+        res = {}
+        for M in (2, 4, 8, 16, 32):
+            x = dev(synth.activations(M, sweep["K"], seed=0, **sweep["act"]))
+            ws = torch.empty(w8.w8a8_linear_workspace_bytes(M, sweep["K"]), dtype=torch.uint8,
+                             device=device)
+            y = torch.empty((M, sweep["N"]), dtype=torch.float16, device=device)
+            xh, sa = w8.quantize_act_per_token_h(x)
+            w8.linear(x, wq, sw, workspace=ws, y=y)
+            w8.w8a8_gemm_h(xh, sa, wq, sw, 0, 8, y)
+            lin_ms = timed(lambda i: w8.linear(x, wq, sw, workspace=ws, y=y))
+
+            def gemm_path(i):
+                w8.quantize_act_per_token_h(x, 0, xh, sa)
+                w8.w8a8_gemm_h(xh, sa, wq, sw, 0, 8, y)
+            gemm_ms = timed(gemm_path)
+            nbytes = sweep["N"] * sweep["K"] + 4 * sweep["N"] + M * (2 * sweep["K"] + 2 * sweep["N"])
+            res[str(M)] = {"linear_us": round(lin_ms * 1e3, 3),
+                           "linear_GBps": round(nbytes / (lin_ms * 1e-3) / 1e9, 1),
+                           "tensor_core_gemm_us": round(gemm_ms * 1e3, 3),
+                           "path": "few-row kernel" if M <= 16 else "tensor-core GEMM"}
+        out["few_rows_N10240_K2560"] = res
+
     wl = synth.WORKLOADS
+    few_rows_case()
     # the 512 x 512 per-channel layer: the whole linear() call
     small = wl["pc_small"]
     x = dev(synth.activations(128, 512, seed=0, **small["act"]))

@@ -377,6 +377,54 @@ def test_w4a8_gemm_output(M, N, K):
     assert_bits(y, ref)
 
 
+# ------------------------------------- few-row products (M = 2..16) ----
+#
+# Two to sixteen activation rows run on the weight stream of the
+# matrix-vector kernel (one weight load, one dp4a per activation row) when
+# their codes fit its shared memory; the outputs are those of the oracle bit
+# for bit.  ("cider 소개", section "cider의 동작 방식과 자동 경로 선택": the
+# seq_len rule leaves the choice open between one token and a GEMM tile.)
+
+SKINNY_CASES = [(2, 257, 512, 8), (3, 1000, 2560, 8), (4, 130, 4096, 8), (5, 300, 2560, 8),
+                (8, 10240, 2560, 8), (13, 129, 4096, 8), (16, 520, 4096, 8), (16, 64, 256, 8),
+                (2, 33, 32768, 8), (7, 100, 8192, 8), (2, 300, 1024, 4), (6, 129, 4096, 4),
+                (16, 14336, 4096, 4), (9, 77, 8192, 4)]
+
+
+@pytest.mark.parametrize("M,N,K,wbits", SKINNY_CASES)
+def test_few_row_products_bit_exact(M, N, K, wbits):
+    x = act(M, K, seed=M * 3 + K, n_outliers=4, outlier_scale=40.0, zero_rows=(M - 1,))
+    W = synth.weights(N, K, seed=N + M)
+    xq, sa = oracle.quantize_act_per_token(x)
+    if wbits == 8:
+        wq, sw = oracle.quantize_weight_int8(W)
+        ref = oracle.dequant(oracle.int_gemm(xq, wq), sa, sw)
+        y = host(w8.w8a8_gemm(dev(xq), dev(sa), dev(wq), dev(sw)))
+    else:
+        wq, sw = oracle.pack_weight_int4(W)
+        ref = oracle.dequant(oracle.int_gemm(xq, oracle.unpack_int4(wq, K)), sa, sw)
+        y = host(w8.w4a8_gemm(dev(xq), dev(sa), dev(wq), dev(sw)))
+    assert_fp16_close(y, ref)
+    assert_bits(y, ref)
+    # the whole layer: the INT8 quantizer, then the same kernel
+    yl = host(w8.linear(dev(x), dev(wq), dev(sw), 0, wbits))
+    assert_bits(yl, oracle.linear(x, wq, sw, 0, wbits))
+
+
+def test_few_row_products_extreme_codes():
+    """All-+-127 activations and weights: the int32 sums reach 127^2 K."""
+    M, N, K = 16, 96, 4096
+    a = np.full((M, K), 127, np.int8)
+    a[1::2] = -127
+    w = np.full((N, K), 127, np.int8)
+    w[::3, ::2] = -127
+    sa = np.full((M, 1), 2.0 ** -7, np.float32)
+    sw = np.full((N, 1), 2.0 ** -10, np.float32)
+    ref = oracle.dequant(oracle.int_gemm(a, w), sa, sw)
+    y = host(w8.w8a8_gemm(dev(a), dev(sa), dev(w), dev(sw)))
+    assert_bits(y, ref)
+
+
 # --------------------------------------------------------- whole layer ----
 
 @pytest.mark.parametrize("M,N,K,gs,wbits", [

@@ -91,6 +91,8 @@ int gemm_dispatch(const int8_t *xq, const float *sa, const void *W,
     return launch_gemv_w8a8(xq, sa, static_cast<const int8_t *>(W), sw, N, K,
                             gs, y, s);
   }
+  // a few rows: the weight stream of the matrix-vector kernel
+  if (skinny_supported(M, K, gs)) return launch_skinny(xq, sa, W, sw, M, N, K, wbits, y, s);
   return launch_gemm_tc(xq, false, sa, W, sw, M, N, K, gs, wbits, y, nullptr, s);
 }
 
@@ -253,6 +255,14 @@ int linear(const w8a8_half *x, const void *Wq, const float *scale_w, int M,
     // decode: one kernel quantizes the row and streams the weights
     return launch_linear_mv(reinterpret_cast<const __half *>(x), Wq, scale_w, N, K, group_size,
                             wbits, reinterpret_cast<__half *>(y), s);
+  }
+  if (skinny_supported(M, K, group_size)) {
+    // a few rows: INT8 codes into the workspace, then the weight stream of
+    // the matrix-vector kernel (launched early; it waits for the codes)
+    int8_t *xq = static_cast<int8_t *>(workspace);
+    W8A8_TRY(launch_row_quant_act(reinterpret_cast<const __half *>(x), M, K, group_size, xq, sa,
+                                  s));
+    return launch_skinny(xq, sa, Wq, scale_w, M, N, K, wbits, reinterpret_cast<__half *>(y), s);
   }
   __half *xq_h = static_cast<__half *>(workspace);
   W8A8_TRY(launch_row_quant_half(reinterpret_cast<const __half *>(x), M, K, group_size, xq_h,

@@ -15,6 +15,13 @@ constexpr int kNumSMsGB300 = 152;
 
 constexpr int kMaxK = 32768;
 
+// Few-row products (2 <= M <= kSkinnyMaxM, per channel) run on the weight
+// stream of the matrix-vector kernel when the activation codes of the
+// padded row count (2, 4, 8 or 16 rows) fit kSkinnyMaxCodeBytes of shared
+// memory; other shapes take the tensor-core GEMM.
+constexpr int kSkinnyMaxM = 16;
+constexpr int kSkinnyMaxCodeBytes = 64 * 1024;
+
 // Reads and clears the device-side error word that kernels with bounded
 // waits set when a wait gives up (the value says which wait).
 int read_and_clear_device_error(unsigned int *code);
@@ -30,6 +37,7 @@ enum DeviceErrorCode : unsigned int {
   kDevErrAccumBarrier = 3,   // epilogue wait on a finished accumulator
   kDevErrTmemEmpty = 4,      // MMA wait on a drained accumulator
   kDevErrSmemAlign = 5,      // dynamic shared memory not 1 KB aligned (kernel did nothing)
+  kDevErrRowCopy = 6,        // decode kernel: bulk copy of the activation row did not land
 };
 
 inline bool aligned16(const void *p) {
@@ -73,6 +81,17 @@ int launch_gemv_w4a8(const int8_t *xq, const float *sa, const uint8_t *Wp,
 // The whole layer for one fp16 row: quantization fused into the MV kernel.
 int launch_linear_mv(const __half *x, const void *W, const float *sw, int N, int K,
                      int group_size, int wbits, __half *y, cudaStream_t s);
+
+// Few-row products: y [M, N] from INT8 codes xq [M, K] (scales sa [M]) and
+// per-channel weights, 2 <= M <= kSkinnyMaxM.
+bool skinny_supported(int M, int K, int group_size);
+int launch_skinny(const int8_t *xq, const float *sa, const void *W, const float *sw, int M, int N,
+                  int K, int wbits, __half *y, cudaStream_t s);
+
+// Activation quantization to INT8 codes that lets the next kernel on the
+// stream launch early (it must wait for this grid before reading the codes).
+int launch_row_quant_act(const __half *x, int R, int K, int group_size, int8_t *q, float *scale,
+                         cudaStream_t s);
 
 // Row quantization writing the INT8 codes as fp16 values.
 int launch_row_quant_half(const __half *x, int R, int K, int group_size, __half *qh,
