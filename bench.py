@@ -379,7 +379,7 @@ def measure_workloads(w8, torch, device, flush_l2, l2_bytes, tflops_peak, hbm_pe
 
     def few_rows_case():
         """M = 2..32 rows of the N=10240, K=2560 layer: linear() (the few-row
-        kernel up to 16 rows, the GEMM above) against the quantizer + the
+        kernel up to 8 rows, the GEMM above) against the quantizer + the
         tensor-core GEMM on the same rows; each call after an L2 flush."""
         sweep = wl["pc_sweep"]
         W = dev(synth.weights(sweep["N"], sweep["K"], seed=0))
@@ -404,10 +404,43 @@ def measure_workloads(w8, torch, device, flush_l2, l2_bytes, tflops_peak, hbm_pe
             res[str(M)] = {"linear_us": round(lin_ms * 1e3, 3),
                            "linear_GBps": round(nbytes / (lin_ms * 1e-3) / 1e9, 1),
                            "tensor_core_gemm_us": round(gemm_ms * 1e3, 3),
-                           "path": "few-row kernel" if M <= 16 else "tensor-core GEMM"}
+                           "path": "few-row kernel" if M <= 8 else "tensor-core GEMM"}
         out["few_rows_N10240_K2560"] = res
 
+    def weight_only_case():
+        """The pages' comparison on this chip: W8A8 per channel (linear(),
+        quantizer included) against the weight-only W8A16 / W4A16 GEMMs (fp16
+        activations) over the N=10240, K=2560 sweep; ratio = weight-only time
+        / W8A8 time, as the pages' PC/w8a16 and PC/w4a16 columns.  M = 1 runs
+        the weight-only product through the tensor-core GEMM (there is no
+        weight-only matrix-vector kernel)."""
+        sweep = wl["pc_sweep"]
+        N, K = sweep["N"], sweep["K"]
+        W = dev(synth.weights(N, K, seed=0))
+        wq, sw = w8.quantize_weight_int8(W)
+        wp, s4 = w8.pack_weight_int4(W)
+        del W
+        res = {}
+        for M in sweep["Ms"]:
+            x = dev(synth.activations(M, K, seed=0, **sweep["act"]))
+            ws = torch.empty(max(w8.w8a8_linear_workspace_bytes(M, K), 1), dtype=torch.uint8,
+                             device=device)
+            y = torch.empty((M, N), dtype=torch.float16, device=device)
+            w8.linear(x, wq, sw, workspace=ws, y=y)
+            w8.weight_only_gemm(x, wq, sw, 0, 8, y)
+            w8.weight_only_gemm(x, wp, s4, 0, 4, y)
+            pc = timed(lambda i: w8.linear(x, wq, sw, workspace=ws, y=y))
+            w16 = timed(lambda i: w8.weight_only_gemm(x, wq, sw, 0, 8, y))
+            w4 = timed(lambda i: w8.weight_only_gemm(x, wp, s4, 0, 4, y))
+            ops = 2.0 * M * N * K
+            res[str(M)] = {"w8a8_pc_ms": round(pc, 5), "w8a16_ms": round(w16, 5),
+                           "w4a16_ms": round(w4, 5),
+                           "w8a16_TFLOPs": round(ops / (w16 * 1e-3) / 1e12, 1),
+                           "pc_over_w8a16": round(w16 / pc, 3), "pc_over_w4a16": round(w4 / pc, 3)}
+        out["weight_only_vs_w8a8_N10240_K2560"] = res
+
     wl = synth.WORKLOADS
+    weight_only_case()
     few_rows_case()
     # the 512 x 512 per-channel layer: the whole linear() call
     small = wl["pc_small"]

@@ -221,6 +221,25 @@ int linear_noalloc(const w8a8_half *x, const void *Wq, const float *scale_w, int
                    int N, int K, int group_size, int wbits, w8a8_half *y,
                    w8a8_stream_t stream);
 
+/* The weight-only product the method is measured against (W8A16 / W4A16:
+ * "Apple Silicon의 AI 한계치는 당신의 생각보다 높습니다", the section on
+ * MLX's weight-only quantization -- integer weights dequantized and
+ * multiplied with fp16 activations; "cider 소개", mode table, W8A16 /
+ * W4A16 rows, and the w8a16 / w4a16 columns of the latency table).  The
+ * activations stay fp16: y = x . (q * s_w)^T, accumulated in fp32 on the
+ * tensor cores (the integer codes are exact fp16 operands), then scaled by
+ * s_w (per group: each group's sum scaled and added in ascending order) and
+ * rounded once to fp16.  Not bit-exact against the double-precision
+ * definition: within |dy| <= 2e-3 * max|y| + one fp16 ulp.
+ *   x        fp16 [M, K]
+ *   Wq       int8 [N, K] (wbits 8) or packed uint8 [N, K/2] (wbits 4, as
+ *            pack_weight_int4 writes them; requires group_size 0)
+ *   scale_w  fp32 [N, G]
+ *   y        fp16 [M, N]       (out)
+ * Any M >= 1 (the tensor-core GEMM, launched like w8a8_gemm_h). */
+int weight_only_gemm(const w8a8_half *x, const void *Wq, const float *scale_w, int M, int N,
+                     int K, int group_size, int wbits, w8a8_half *y, w8a8_stream_t stream);
+
 /* Test export of step 3 alone ("INT8 TensorOps 커널 설계": INT32
  * accumulation): acc[m, n, g] = sum over k in group g of xq[m, k] *
  * Wq[n, k], exact, as int32 [M, N, G], through the same tensor-core

@@ -95,6 +95,12 @@ def test_argument_errors_before_any_launch(lib):
     assert gh(A16, C16, B16, C16, 4, 8, 64, 64, 4, D16, S0) == INV     # W4 per group
     assert gh(ODD, C16, B16, C16, 4, 8, 64, 0, 8, D16, S0) == MIS
     assert lib.quantize_act_per_token_h(A16, 4, 40, 0, B16, C16, S0) == MIS
+    wo = lib.weight_only_gemm
+    assert wo(A16, B16, C16, 4, 8, 64, 0, 5, D16, S0) == INV      # wbits
+    assert wo(A16, B16, C16, 4, 8, 64, 64, 4, D16, S0) == INV     # W4 per group
+    assert wo(A16, B16, C16, 4, 8, 48, 0, 4, D16, S0) == MIS      # K % 32 for INT4
+    assert wo(ODD, B16, C16, 4, 8, 64, 0, 8, D16, S0) == MIS
+    assert wo(A16, B16, C16, 0, 8, 64, 0, 8, D16, S0) == 0        # empty problem
     i32 = lib.w8a8_gemm_i32
     assert i32(A16, B16, 4, 8, 64, 0, 5, C16, S0) == INV
     assert i32(A16, B16, 4, 8, 64, 64, 4, C16, S0) == INV

@@ -379,10 +379,10 @@ def test_w4a8_gemm_output(M, N, K):
 
 # ------------------------------------- few-row products (M = 2..16) ----
 #
-# Two to sixteen activation rows run on the weight stream of the
-# matrix-vector kernel (one weight load, one dp4a per activation row) when
-# their codes fit its shared memory; the outputs are those of the oracle bit
-# for bit.  ("cider 소개", section "cider의 동작 방식과 자동 경로 선택": the
+# Two to eight activation rows run on the weight stream of the matrix-vector
+# kernel (one weight load, one dp4a per activation row) when their codes fit
+# its shared memory, more rows on the tensor-core GEMM; the outputs are
+# those of the oracle bit for bit on either side of that boundary.  ("cider 소개", section "cider의 동작 방식과 자동 경로 선택": the
 # seq_len rule leaves the choice open between one token and a GEMM tile.)
 
 SKINNY_CASES = [(2, 257, 512, 8), (3, 1000, 2560, 8), (4, 130, 4096, 8), (5, 300, 2560, 8),
@@ -422,6 +422,46 @@ def test_few_row_products_extreme_codes():
     sw = np.full((N, 1), 2.0 ** -10, np.float32)
     ref = oracle.dequant(oracle.int_gemm(a, w), sa, sw)
     y = host(w8.w8a8_gemm(dev(a), dev(sa), dev(w), dev(sw)))
+    assert_bits(y, ref)
+
+
+# ------------------------------- weight-only W8A16 / W4A16 (the baseline) ----
+#
+# fp16 activations times the dequantized weights, float accumulation on the
+# tensor cores; against the oracle's exact product rounded once, within the
+# fp16 tolerance ("Apple Silicon의 AI 한계치는 …", MLX weight-only section;
+# "cider 소개", W8A16 / W4A16 rows of the mode table).
+
+WONLY_CASES = [(130, 257, 512, 0, 8), (257, 130, 2560, 128, 8), (300, 129, 4096, 64, 8),
+               (129, 520, 14336, 0, 8), (2, 3, 16, 0, 8), (1, 300, 2560, 0, 8),
+               (300, 257, 4096, 0, 4), (5, 1000, 2560, 0, 4), (513, 384, 2560, 64, 8),
+               (64, 64, 32768, 0, 8)]
+
+
+@pytest.mark.parametrize("M,N,K,gs,wbits", WONLY_CASES)
+def test_weight_only_matches_oracle(M, N, K, gs, wbits):
+    x = act(M, K, seed=K + M, n_outliers=4, outlier_scale=40.0, zero_rows=(M - 1,))
+    W = synth.weights(N, K, seed=N + 11)
+    if wbits == 8:
+        wq, sw = oracle.quantize_weight_int8(W, gs)
+    else:
+        wq, sw = oracle.pack_weight_int4(W)
+    ref = oracle.linear_weight_only(x, wq, sw, gs, wbits)
+    y = host(w8.weight_only_gemm(dev(x), dev(wq), dev(sw), gs, wbits))
+    assert_fp16_close(y, ref)
+    assert np.all(y[M - 1] == 0)  # a zero row gives zero outputs
+
+
+def test_weight_only_exact_cases():
+    """Integer x with power-of-two scales: every product, sum and scaling is
+    exact in fp32, so the output equals the oracle bit for bit."""
+    rng = np.random.default_rng(21)
+    M, N, K = 130, 257, 1024
+    x = rng.integers(-8, 9, size=(M, K)).astype(np.float16)
+    q = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    sw = (2.0 ** -rng.integers(10, 14, size=(N, 1))).astype(np.float32)
+    ref = oracle.weight_only(x, q, sw)
+    y = host(w8.weight_only_gemm(dev(x), dev(q), dev(sw)))
     assert_bits(y, ref)
 
 

@@ -30,7 +30,7 @@ EXPORTS = ("w8a8_is_available", "w8a8_status_string", "w8a8_check_status",
            "quantize_weight_int8", "pack_weight_int4", "quantize_act_per_token",
            "w8a8_gemm", "w8a8_mv", "w4a8_gemm", "quantize_act_per_token_h", "w8a8_gemm_h",
            "w8a8_linear_workspace_bytes", "linear", "linear_noalloc", "w8a8_gemm_i32",
-           "w8a8_test_set_fault")
+           "w8a8_test_set_fault", "weight_only_gemm")
 
 
 class W8A8Error(RuntimeError):
@@ -68,6 +68,7 @@ def load(path: str | None = None):
             "linear_noalloc": ([P, P, P, I, I, I, I, I, P, P], I),
             "w8a8_gemm_i32": ([P, P, I, I, I, I, I, P, P], I),
             "w8a8_test_set_fault": ([ctypes.c_longlong, I], I),
+            "weight_only_gemm": ([P, P, P, I, I, I, I, I, P, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -281,6 +282,24 @@ def linear_noalloc(x, Wq, scale_w, group_size: int = 0, wbits: int = 8, y=None):
     _need(y, torch.float16, "y", (M, N))
     _check(load().linear_noalloc(_ptr(x), _ptr(Wq), _ptr(scale_w), M, N, K, group_size, wbits,
                                  _ptr(y), _stream()), "linear_noalloc")
+    return y
+
+
+def weight_only_gemm(x, Wq, scale_w, group_size: int = 0, wbits: int = 8, y=None):
+    """Weight-only product (W8A16 / W4A16): fp16 x [M, K] times the dequantized
+    weights (int8 Wq [N, K], or packed uint8 [N, K/2] with wbits 4)."""
+    _need(x, torch.float16, "x")
+    M, K = x.shape
+    wdtype = torch.int8 if wbits == 8 else torch.uint8
+    _need(Wq, wdtype, "Wq")
+    N = Wq.shape[0]
+    if Wq.shape[1] * (1 if wbits == 8 else 2) != K:
+        raise ValueError("Wq inner dimension does not match K")
+    _need(scale_w, torch.float32, "scale_w", (N, _groups(K, group_size)))
+    y = torch.empty((M, N), dtype=torch.float16, device=x.device) if y is None else y
+    _need(y, torch.float16, "y", (M, N))
+    _check(load().weight_only_gemm(_ptr(x), _ptr(Wq), _ptr(scale_w), M, N, K, group_size, wbits,
+                                   _ptr(y), _stream()), "weight_only_gemm")
     return y
 
 

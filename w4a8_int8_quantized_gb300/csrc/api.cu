@@ -271,6 +271,20 @@ int linear(const w8a8_half *x, const void *Wq, const float *scale_w, int M,
                          reinterpret_cast<__half *>(y), s);
 }
 
+int weight_only_gemm(const w8a8_half *x, const void *Wq, const float *scale_w, int M, int N,
+                     int K, int group_size, int wbits, w8a8_half *y, w8a8_stream_t stream) {
+  if (wbits != 8 && wbits != 4) return W8A8_ERR_INVALID_ARG;
+  if (wbits == 4 && group_size != 0) return W8A8_ERR_INVALID_ARG;
+  W8A8_TRY(check_shape(M, N, K, group_size, wbits == 4 ? 32 : 16));
+  if (M == 0 || N == 0) return W8A8_OK;
+  W8A8_TRY(check_ptrs16({x, Wq, y}));
+  W8A8_TRY(check_ptrs4({scale_w}));
+  W8A8_TRY(check_device());
+  return launch_gemm_weight_only(reinterpret_cast<const __half *>(x), Wq, scale_w, M, N, K,
+                                 group_size, wbits, reinterpret_cast<__half *>(y),
+                                 as_stream(stream));
+}
+
 int w8a8_gemm_i32(const int8_t *xq, const void *Wq, int M, int N, int K,
                   int group_size, int wbits, int32_t *acc,
                   w8a8_stream_t stream) {

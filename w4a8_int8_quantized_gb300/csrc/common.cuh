@@ -17,9 +17,11 @@ constexpr int kMaxK = 32768;
 
 // Few-row products (2 <= M <= kSkinnyMaxM, per channel) run on the weight
 // stream of the matrix-vector kernel when the activation codes of the
-// padded row count (2, 4, 8 or 16 rows) fit kSkinnyMaxCodeBytes of shared
-// memory; other shapes take the tensor-core GEMM.
-constexpr int kSkinnyMaxM = 16;
+// padded row count (2, 4 or 8 rows) fit kSkinnyMaxCodeBytes of shared
+// memory; other shapes take the tensor-core GEMM.  Measured at N=10240,
+// K=2560 after an L2 flush: 14 / 18 / 27 us at 2 / 4 / 8 rows against 27-31
+// us for the GEMM, and 43 us at 16 rows (dp4a-bound), hence the limit of 8.
+constexpr int kSkinnyMaxM = 8;
 constexpr int kSkinnyMaxCodeBytes = 64 * 1024;
 
 // Reads and clears the device-side error word that kernels with bounded
@@ -103,5 +105,11 @@ int launch_row_quant_half(const __half *x, int R, int K, int group_size, __half 
 int launch_gemm_tc(const void *A, bool a_half, const float *sa, const void *W,
                    const float *sw, int M, int N, int K, int group_size, int wbits,
                    __half *y, int32_t *acc_out, cudaStream_t s);
+
+// Weight-only product on the tensor cores: fp16 x [M, K] times the integer
+// weight codes, float accumulation, y = fp16(acc * s_w) (per group: the
+// groups' sums rescaled and added in ascending order).
+int launch_gemm_weight_only(const __half *x, const void *W, const float *sw, int M, int N, int K,
+                            int group_size, int wbits, __half *y, cudaStream_t s);
 
 }  // namespace w8a8

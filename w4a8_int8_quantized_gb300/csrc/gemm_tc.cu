@@ -224,25 +224,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   return d;
 }
 
-// 32 consecutive TMEM columns of this thread's lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-        "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
-        "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),
-        "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
-        "=r"(v[30]), "=r"(v[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // Ordered memory accesses for the epilogue: as volatile asm they keep their
 // program order, so a fully unrolled loop does not hoist all of its loads
 // ahead of its stores (which would need one register per load).
@@ -392,45 +373,87 @@ __device__ __forceinline__ void convert_sub(const uint8_t *src, uint8_t *dst, in
   }
 }
 
+// 32 consecutive TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+        "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+        "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]),
+        "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+        "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+// Waits for this thread's TMEM loads; the loaded registers pass through the
+// statement, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]),
+                 "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),
+                 "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]),
+                 "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+}
+
 // Epilogue of the tensor-core GEMM (warps 8-15): drains the TMEM
-// accumulators chunk by chunk, sums them exactly (int32) or rescales each
-// group (fp32), then writes fp16 y.  The accumulator of a tile holds 128
-// output channels (TMEM lanes) x BT tokens (columns); warp 8 + 4h + q owns
-// lane quadrant q and tokens [h BT/2, (h+1) BT/2).  Tiles are
-// tile0, tile0 + tile_step, ...; tile t covers channels
-// (t % nblocks) * ch_block + ch_off + [0, 128) and tokens (t / nblocks) * BT
-// + [0, BT).  Each warp arrives on accempty0 (+8 per accumulator) when its
-// share of a chunk is drained.
-template <bool PERGROUP, int BT>
+// accumulators chunk by chunk and writes fp16 y.  The accumulator of a tile
+// holds 128 output channels (TMEM lanes) x BT tokens (columns); warp 8 + 4h
+// + q owns lane quadrant q and tokens [h BT/2, (h+1) BT/2).  Tiles are
+// tile0, tile0 + tile_step, ...; tile t covers channels (t % nblocks) *
+// ch_block + ch_off + [0, 128) and tokens (t / nblocks) * BT + [0, BT).
+// Each warp arrives on accempty0 (+8 per accumulator) when its share of a
+// chunk is drained.  The columns of a chunk are read 32 at a time, each
+// slice finished before the next is loaded (one slice live keeps the
+// register count within the epilogue's share; loading the next slice early,
+// 16 columns at a time, measured slower per group).  Modes:
+//   exact per channel: each chunk is converted to int32 (exact) and summed
+//     in integer; y = fp16(float(sum) * (s_a * s_w));
+//   exact per group: each group is rescaled in fp32 and accumulated in
+//     ascending order, f += acc_g * (s_a,g * s_w,g) (the scale products two
+//     at a time by a paired multiply; the oracle's rounding sequence);
+//     y = fp16(f);
+//   weight-only (WONLY, fp16 activations): one float accumulation over K,
+//     y = fp16(acc * s_w), or per group f += acc_g * s_w,g.
+template <bool PERGROUP, bool WONLY, int BT>
 __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, uint32_t base,
                                               uint8_t *sm, int off_sa, int warp, int lane,
                                               int tile0, int tile_step, int nblocks, int ch_block,
                                               int ch_off, uint32_t accfull0, uint32_t accempty0,
                                               uint32_t saready0, volatile int *abort_flag) {
   constexpr int CPT = BT / 2;  // token columns per epilogue thread
+  // activation scales are staged per tile (per channel) or per group
+  constexpr bool STAGE_SA = !WONLY;
   const int nkb = p.nkb, chunk_kb = p.chunk_kb;
   auto accfull = [&](uint32_t r) { return accfull0 + 8u * r; };
   auto accempty = [&](uint32_t r) { return accempty0 + 8u * r; };
   auto saready = [&](uint32_t b) { return saready0 + 8u * b; };
-    const int q = warp & 3;             // TMEM lane quadrant of this warp
-    const int et = (warp - 8) * 32 + lane;
-    const int half = (warp - 8) >> 2;   // which half of the BT token columns
-    const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t sas = base + off_sa;
-    float *sas_ptr = reinterpret_cast<float *>(sm + off_sa);
-    const bool want_y = p.acc_out == nullptr;
-    uint32_t cc = 0, su = 0;  // chunks drained, scale buffers used
-    bool ok = true;
-    for (int tile = tile0; tile < p.ntiles && ok; tile += tile_step) {
-      const int nb = tile % nblocks, tb = tile / nblocks;
-      // this thread's channel
-      const long n = static_cast<long>(nb) * ch_block + ch_off + q * 32 + lane;
-      const long mtile = static_cast<long>(tb) * BT;
-      const long m0 = mtile + half * CPT;                           // its first token
-      // per channel: stage the tile's BT activation scales now, used at the end
-      uint32_t sb = 0, sph = 0;
-      float swn = 0.f;
-      if (!PERGROUP && want_y) {
+  const int q = warp & 3;             // TMEM lane quadrant of this warp
+  const int et = (warp - 8) * 32 + lane;
+  const int half = (warp - 8) >> 2;   // which half of the BT token columns
+  const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  const uint32_t sas = base + off_sa;
+  float *sas_ptr = reinterpret_cast<float *>(sm + off_sa);
+  const bool want_y = p.acc_out == nullptr;
+  uint32_t cc = 0, su = 0;  // chunks drained, scale buffers used
+  bool ok = true;
+  for (int tile = tile0; tile < p.ntiles && ok; tile += tile_step) {
+    const int nb = tile % nblocks, tb = tile / nblocks;
+    // this thread's channel
+    const long n = static_cast<long>(nb) * ch_block + ch_off + q * 32 + lane;
+    const long mtile = static_cast<long>(tb) * BT;
+    const long m0 = mtile + half * CPT;                           // its first token
+    // per channel: stage the tile's BT activation scales now, used at the end
+    uint32_t sb = 0, sph = 0;
+    float swn = 0.f;
+    if (!PERGROUP && want_y) {
+      if (STAGE_SA) {
         sb = su & 1u;
         sph = (su >> 1) & 1u;
         ++su;
@@ -439,17 +462,19 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
           sas_ptr[sb * BT + et] = m < p.M ? __ldg(p.sa + m) : 0.f;
         }
         mbar_arrive(saready(sb));
-        if (n < p.N) swn = __ldg(p.sw + n);
       }
-      uint32_t acc[CPT];  // int32 sums (per channel) or fp32 totals (per group)
+      if (n < p.N) swn = __ldg(p.sw + n);
+    }
+    uint32_t acc[CPT];  // int32 sums (exact per channel) or fp32 totals
 #pragma unroll
-      for (int i = 0; i < CPT; ++i) acc[i] = 0u;
-      const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
-      for (int c = 0; c < nchunks; ++c) {
-        const uint32_t r = cc & 1u;
-        float sw_g = 0.f;
-        uint32_t gb = 0, gph = 0;
-        if (PERGROUP && want_y) {
+    for (int i = 0; i < CPT; ++i) acc[i] = 0u;
+    const int nchunks = (nkb + chunk_kb - 1) / chunk_kb;
+    for (int c = 0; c < nchunks; ++c) {
+      const uint32_t r = cc & 1u;
+      float sw_g = 0.f;
+      uint32_t gb = 0, gph = 0;
+      if (PERGROUP && want_y) {
+        if (STAGE_SA) {
           // stage group c's activation scales for the BT tokens
           gb = su & 1u;
           gph = (su >> 1) & 1u;
@@ -459,121 +484,136 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
             sas_ptr[gb * BT + et] = m < p.M ? __ldg(p.sa + m * p.G + c) : 0.f;
           }
           mbar_arrive(saready(gb));
-          if (n < p.N) sw_g = __ldg(p.sw + n * p.G + c);
         }
-        bool w = wait_bar(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
-        if (PERGROUP && want_y)
-          w = w && wait_bar(saready(gb), gph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
-        if (!__all_sync(0xffffffffu, w)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        if (n < p.N) sw_g = __ldg(p.sw + n * p.G + c);
+      }
+      bool w = wait_bar(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err,
+                        p.wait_limit);
+      if (PERGROUP && want_y && STAGE_SA)
+        w = w && wait_bar(saready(gb), gph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t col0 = tq + r * BT + half * CPT;
 #pragma unroll
-        for (int j = 0; j < CPT / 32; ++j) {
-          uint32_t v[32];
-          tmem_ld32(tq + r * BT + half * CPT + j * 32, v);
-          tmem_wait_ld();
-          if (PERGROUP) {
-            if (want_y) {
+      for (int j = 0; j < CPT / 32; ++j) {
+        uint32_t v[32];
+        tmem_ld32(col0 + j * 32, v);
+        tmem_wait_ld32(v);
+        if (PERGROUP) {
+          if (want_y) {
 #pragma unroll
-              for (int i4 = 0; i4 < 8; ++i4) {
-                const float4 s4 =
-                    lds_f32x4(sas + (gb * BT + half * CPT + j * 32 + i4 * 4) * 4);
-                float sc[4];
+            for (int i4 = 0; i4 < 8; ++i4) {
+              float sc[4];
+              if (WONLY) {
+                sc[0] = sc[1] = sc[2] = sc[3] = sw_g;
+              } else {
+                const float4 s4 = lds_f32x4(sas + (gb * BT + half * CPT + j * 32 + i4 * 4) * 4);
                 mul2(s4.x, s4.y, sw_g, sc[0], sc[1]);  // (s_a * s_w) first, as in the dequant rule
                 mul2(s4.z, s4.w, sw_g, sc[2], sc[3]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int idx = j * 32 + i4 * 4 + e;
-                  acc[idx] = __float_as_uint(__fadd_rn(
-                      __uint_as_float(acc[idx]), __fmul_rn(__uint_as_float(v[i4 * 4 + e]), sc[e])));
-                  asm volatile("" : "+r"(acc[idx]));  // before the next scale load
-                }
               }
-            } else if (n < p.N) {
-              // export of the exact group partials; sequential addresses
-              int32_t *ap = p.acc_out + ((m0 + j * 32) * p.N + n) * p.G + c;
-              const long step = static_cast<long>(p.N) * p.G;
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                if (m0 + j * 32 + i < p.M) stg_b32(ap, __float2int_rn(__uint_as_float(v[i])));
-                ap += step;
-                asm volatile("" : "+l"(ap));
+              for (int e = 0; e < 4; ++e) {
+                const int idx = j * 32 + i4 * 4 + e;
+                acc[idx] = __float_as_uint(__fadd_rn(
+                    __uint_as_float(acc[idx]), __fmul_rn(__uint_as_float(v[i4 * 4 + e]), sc[e])));
+                asm volatile("" : "+r"(acc[idx]));  // before the next scale load
               }
             }
-          } else {
+          } else if (n < p.N) {
+            // export of the exact group partials; sequential addresses
+            int32_t *ap = p.acc_out + ((m0 + j * 32) * p.N + n) * p.G + c;
+            const long step = static_cast<long>(p.N) * p.G;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const int idx = j * 32 + i;
-              acc[idx] = static_cast<uint32_t>(static_cast<int>(acc[idx]) +
-                                               __float2int_rn(__uint_as_float(v[i])));
+              if (m0 + j * 32 + i < p.M) stg_b32(ap, __float2int_rn(__uint_as_float(v[i])));
+              ap += step;
+              asm volatile("" : "+l"(ap));
             }
           }
-          // finish this slice before the next TMEM load (keeps one slice live)
+        } else if (WONLY) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(acc[j * 32 + i]));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(accempty(r));
-        ++cc;
-      }
-      if (!ok) break;
-      if (!want_y) {
-        if (!PERGROUP && n < p.N) {
-          int32_t *ap = p.acc_out + m0 * p.N + n;
+          for (int i = 0; i < 32; ++i) {
+            const int idx = j * 32 + i;
+            acc[idx] = __float_as_uint(__fadd_rn(__uint_as_float(acc[idx]), __uint_as_float(v[i])));
+          }
+        } else {
 #pragma unroll
-          for (int i = 0; i < CPT; ++i) {
-            if (m0 + i < p.M) stg_b32(ap, static_cast<int>(acc[i]));
-            ap += p.N;
-            asm volatile("" : "+l"(ap));
+          for (int i = 0; i < 32; ++i) {
+            const int idx = j * 32 + i;
+            acc[idx] = static_cast<uint32_t>(static_cast<int>(acc[idx]) +
+                                             __float2int_rn(__uint_as_float(v[i])));
           }
         }
-        continue;
-      }
-      if (!PERGROUP) {
-        bool w = wait_bar(saready(sb), sph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
-        if (!__all_sync(0xffffffffu, w)) break;
-      }
-      if (n >= p.N) continue;
-      // y[m, n] for this thread's channel n and tokens m0 .. m0 + CPT - 1: a
-      // warp store covers 32 consecutive channels (64 contiguous bytes).  The
-      // row pointer advances by N per token; the empty asm keeps the compiler
-      // from precomputing all CPT addresses at once.
-      __half *yp = p.y + m0 * p.N + n;
-      const int mcount = static_cast<int>(min(static_cast<long>(CPT), p.M - m0));
+        // finish this slice before the next TMEM load (keeps one slice live)
 #pragma unroll
-      for (int i4 = 0; i4 < CPT / 4; ++i4) {
-        float sv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (!PERGROUP) {
-          const float4 s4 = lds_f32x4(sas + (sb * BT + half * CPT + i4 * 4) * 4);
-          sv[0] = s4.x;
-          sv[1] = s4.y;
-          sv[2] = s4.z;
-          sv[3] = s4.w;
-        }
+        for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(acc[j * 32 + i]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty(r));
+      ++cc;
+    }
+    if (!ok) break;
+    if (!want_y) {
+      if (!PERGROUP && n < p.N) {
+        int32_t *ap = p.acc_out + m0 * p.N + n;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = i4 * 4 + e;
-          if (i < mcount) {
-            const float o =
-                PERGROUP ? __uint_as_float(acc[i])
-                         : __fmul_rn(static_cast<float>(static_cast<int>(acc[i])),
-                                     __fmul_rn(sv[e], swn));
-            stg_b16(yp, __float2half_rn(o));
-          }
-          yp += p.N;
-          asm volatile("" : "+l"(yp));
+        for (int i = 0; i < CPT; ++i) {
+          if (m0 + i < p.M) stg_b32(ap, static_cast<int>(acc[i]));
+          ap += p.N;
+          asm volatile("" : "+l"(ap));
         }
+      }
+      continue;
+    }
+    if (!PERGROUP && STAGE_SA) {
+      bool w = wait_bar(saready(sb), sph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
+      if (!__all_sync(0xffffffffu, w)) break;
+    }
+    if (n >= p.N) continue;
+    // y[m, n] for this thread's channel n and tokens m0 .. m0 + CPT - 1: a
+    // warp store covers 32 consecutive channels (64 contiguous bytes).  The
+    // row pointer advances by N per token; the empty asm keeps the compiler
+    // from precomputing all CPT addresses at once.
+    __half *yp = p.y + m0 * p.N + n;
+    const int mcount = static_cast<int>(min(static_cast<long>(CPT), p.M - m0));
+#pragma unroll
+    for (int i4 = 0; i4 < CPT / 4; ++i4) {
+      float sv[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!PERGROUP && !WONLY) {
+        const float4 s4 = lds_f32x4(sas + (sb * BT + half * CPT + i4 * 4) * 4);
+        sv[0] = s4.x;
+        sv[1] = s4.y;
+        sv[2] = s4.z;
+        sv[3] = s4.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = i4 * 4 + e;
+        if (i < mcount) {
+          float o;
+          if (PERGROUP)
+            o = __uint_as_float(acc[i]);
+          else if (WONLY)
+            o = __fmul_rn(__uint_as_float(acc[i]), swn);
+          else
+            o = __fmul_rn(static_cast<float>(static_cast<int>(acc[i])), __fmul_rn(sv[e], swn));
+          stg_b16(yp, __float2half_rn(o));
+        }
+        yp += p.N;
+        asm volatile("" : "+l"(yp));
       }
     }
+  }
   tc_fence_before();
 }
 
 // ------------------------------------------------------------- kernel ----
 
-template <int WBITS, bool PERGROUP, bool XH, int BT, int KS>
+template <int WBITS, bool PERGROUP, bool XH, int BT, int KS, bool WONLY>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmW, const TcParams p) {
@@ -652,7 +692,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // allocates registers to that limit.
   if (warp >= 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;");
-    epilogue_role<PERGROUP, BT>(p, tmem, base, sm, PL::OFF_SA, warp, lane, blockIdx.x,
+    epilogue_role<PERGROUP, WONLY, BT>(p, tmem, base, sm, PL::OFF_SA, warp, lane, blockIdx.x,
                                        gridDim.x, p.nblocks, BW, 0, accfull(0), accempty(0),
                                        saready(0), abort_flag);
     tc_fence_before();
@@ -875,7 +915,7 @@ bool make_map(CUtensorMap *map, const void *ptr, long rows, long cols, int elem_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int WBITS, bool PERGROUP, bool XH, int BT, int KS>
+template <int WBITS, bool PERGROUP, bool XH, int BT, int KS, bool WONLY = false>
 int launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, cudaStream_t s) {
   // per device: the shared-memory attribute set once, and the SM count
   static bool attr_set[64] = {};
@@ -888,7 +928,7 @@ int launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, cu
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev]) {
-      if (cudaFuncSetAttribute(gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS>,
+      if (cudaFuncSetAttribute(gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS, WONLY>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return W8A8_ERR_CUDA;
       if (cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -908,7 +948,7 @@ int launch_t(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p, cu
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS>, tx, tw, p) !=
+  if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<WBITS, PERGROUP, XH, BT, KS, WONLY>, tx, tw, p) !=
       cudaSuccess) {
     cudaGetLastError();
     return W8A8_ERR_CUDA;
@@ -924,14 +964,13 @@ int launch_modes(const CUtensorMap &tx, const CUtensorMap &tw, const TcParams &p
   return launch_t<8, false, XH, BT, 1>(tx, tw, p, s);
 }
 
-}  // namespace
-
-// X (activations) is int8 codes [M, K] (x_half false) or the same codes as
-// fp16 values (x_half true).  256-token tiles for fp16 codes with M > 128,
-// else 128; per channel with fp16 codes, a stage holds two K blocks.
-int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, const float *sw,
-                   int M, int N, int K, int group_size, int wbits, __half *y,
-                   int32_t *acc_out, cudaStream_t s) {
+// X (activations) is int8 codes [M, K] (x_half false), the same codes as
+// fp16 values (x_half true) or, for the weight-only product (wonly), the
+// fp16 activations themselves.  256-token tiles for fp16 operands with M >
+// 128, else 128; per channel with fp16 operands, a stage holds two K blocks.
+int launch_gemm_any(const void *X, bool x_half, bool wonly, const float *sa, const void *W,
+                    const float *sw, int M, int N, int K, int group_size, int wbits, __half *y,
+                    int32_t *acc_out, cudaStream_t s) {
   // INT8 activation codes are converted in the kernel too: 128-token tiles
   const int bt = (M <= 128 || !x_half) ? 128 : 256;
   const int ks = (x_half && group_size == 0) ? 2 : 1;
@@ -952,9 +991,13 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
   p.gs = group_size;
   p.G = groups_of(K, group_size);
   p.nkb = (K + kb - 1) / kb;  // stages per tile
-  // stages per exact fp32 chunk (see the header comment)
+  // stages per accumulator drain: per group, every group; exact per
+  // channel, every chunk that keeps the fp32 sums exact (see the header
+  // comment); weight-only per channel, once (float accumulation)
   if (group_size != 0)
     p.chunk_kb = group_size / kb;
+  else if (wonly)
+    p.chunk_kb = p.nkb;
   else
     p.chunk_kb = wbits == 8 ? 1024 / kb : 16384 / kb;
   p.nblocks = (N + BW - 1) / BW;
@@ -969,6 +1012,17 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
   p.err = err;
   p.wait_limit = g_wait_limit.load();
   p.skip_first_copy = g_skip_first_copy.load();
+  if (wonly) {
+    if (ks == 2) {
+      if (bt == 128)
+        return wbits == 4 ? launch_t<4, false, true, 128, 2, true>(tx, tw, p, s)
+                          : launch_t<8, false, true, 128, 2, true>(tx, tw, p, s);
+      return wbits == 4 ? launch_t<4, false, true, 256, 2, true>(tx, tw, p, s)
+                        : launch_t<8, false, true, 256, 2, true>(tx, tw, p, s);
+    }
+    if (bt == 128) return launch_t<8, true, true, 128, 1, true>(tx, tw, p, s);
+    return launch_t<8, true, true, 256, 1, true>(tx, tw, p, s);
+  }
   if (x_half) {
     if (ks == 2) {
       if (bt == 128)
@@ -981,6 +1035,20 @@ int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, c
     return launch_t<8, true, true, 256, 1>(tx, tw, p, s);
   }
   return launch_modes<false, 128>(tx, tw, p, wbits, s);
+}
+
+}  // namespace
+
+int launch_gemm_tc(const void *X, bool x_half, const float *sa, const void *W, const float *sw,
+                   int M, int N, int K, int group_size, int wbits, __half *y,
+                   int32_t *acc_out, cudaStream_t s) {
+  return launch_gemm_any(X, x_half, false, sa, W, sw, M, N, K, group_size, wbits, y, acc_out, s);
+}
+
+int launch_gemm_weight_only(const __half *x, const void *W, const float *sw, int M, int N, int K,
+                            int group_size, int wbits, __half *y, cudaStream_t s) {
+  return launch_gemm_any(x, true, true, nullptr, W, sw, M, N, K, group_size, wbits, y, nullptr,
+                         s);
 }
 
 }  // namespace w8a8

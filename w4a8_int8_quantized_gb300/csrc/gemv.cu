@@ -1,4 +1,4 @@
-// Matrix-vector kernels for decode (M == 1) and few-row products (M = 2..16):
+// Matrix-vector kernels for decode (M == 1) and few-row products (M = 2..8):
 // W8A8 per channel / per group and W4A8 per channel; for M == 1 optionally
 // fused with the activation quantization.
 //
@@ -629,7 +629,7 @@ int launch_linear_mv(const __half *x, const void *W, const float *sw, int N, int
   return launch_mv<8, false, true, 1>(x, nullptr, W, sw, 1, N, K, 0, y, s);
 }
 
-int skinny_rows(int M) { return M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+int skinny_rows(int M) { return M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
 bool skinny_supported(int M, int K, int group_size) {
   return M >= 2 && M <= kSkinnyMaxM && group_size == 0 &&
@@ -645,12 +645,9 @@ int launch_skinny(const int8_t *xq, const float *sa, const void *W, const float 
     case 4:
       return wbits == 4 ? launch_rows<4, 4>(xq, sa, W, sw, M, N, K, y, s)
                         : launch_rows<8, 4>(xq, sa, W, sw, M, N, K, y, s);
-    case 8:
+    default:
       return wbits == 4 ? launch_rows<4, 8>(xq, sa, W, sw, M, N, K, y, s)
                         : launch_rows<8, 8>(xq, sa, W, sw, M, N, K, y, s);
-    default:
-      return wbits == 4 ? launch_rows<4, 16>(xq, sa, W, sw, M, N, K, y, s)
-                        : launch_rows<8, 16>(xq, sa, W, sw, M, N, K, y, s);
   }
 }
 
