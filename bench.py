@@ -439,7 +439,37 @@ def measure_workloads(w8, torch, device, flush_l2, l2_bytes, tflops_peak, hbm_pe
                            "pc_over_w8a16": round(w16 / pc, 3), "pc_over_w4a16": round(w4 / pc, 3)}
         out["weight_only_vs_w8a8_N10240_K2560"] = res
 
+    def in_gemm_conversion_case():
+        """What quantization fused into the prefill GEMM would cost: the GEMM
+        fed INT8 activation codes that its converter warps turn into fp16
+        operands in shared memory (every weight tile re-converts the token
+        tile) against the layer's path (fp16 codes straight to the MMA by
+        TMA), at M = 8192 of the N=10240, K=2560 layer; each with its
+        quantizer."""
+        sweep = wl["pc_sweep"]
+        M, N, K = 8192, sweep["N"], sweep["K"]
+        x = dev(synth.activations(M, K, seed=0, **sweep["act"]))
+        W = dev(synth.weights(N, K, seed=0))
+        wq, sw = w8.quantize_weight_int8(W)
+        del W
+        y = torch.empty((M, N), dtype=torch.float16, device=device)
+        xq, sa = w8.quantize_act_per_token(x)
+        xh, sah = w8.quantize_act_per_token_h(x)
+        w8.w8a8_gemm(xq, sa, wq, sw, 0, y)
+        w8.w8a8_gemm_h(xh, sah, wq, sw, 0, 8, y)
+        g8 = timed(lambda i: w8.w8a8_gemm(xq, sa, wq, sw, 0, y))
+        g16 = timed(lambda i: w8.w8a8_gemm_h(xh, sah, wq, sw, 0, 8, y))
+        q8 = timed(lambda i: w8.quantize_act_per_token(x, 0, xq, sa))
+        q16 = timed(lambda i: w8.quantize_act_per_token_h(x, 0, xh, sah))
+        ops = 2.0 * M * N * K
+        out["activation_conversion_in_gemm_M8192"] = {
+            "int8_codes_converted_in_gemm": {"gemm_ms": round(g8, 5), "quant_ms": round(q8, 5),
+                                             "gemm_TOPS": round(ops / (g8 * 1e-3) / 1e12, 1)},
+            "fp16_codes_by_tma": {"gemm_ms": round(g16, 5), "quant_ms": round(q16, 5),
+                                  "gemm_TOPS": round(ops / (g16 * 1e-3) / 1e12, 1)}}
+
     wl = synth.WORKLOADS
+    in_gemm_conversion_case()
     weight_only_case()
     few_rows_case()
     # the 512 x 512 per-channel layer: the whole linear() call

@@ -187,11 +187,14 @@ size_t w8a8_linear_workspace_bytes(int M, int K, int group_size);
 
 /* The whole layer, CiderLinear's forward ("cider 소개", section "cider의
  * 동작 방식과 자동 경로 선택": seq_len > 1 -> INT8 GEMM, seq_len == 1 ->
- * INT8 MV kernel).  M > 1: quantize x per token into the workspace
- * (quantize_act_per_token_h), then the GEMM (w8a8_gemm_h) with the fused
- * dequant.  M == 1: one kernel quantizes the row (same rule) and runs the
- * matrix-vector product with the fused dequant; the workspace is checked
- * but not written (see w8a8_mv for the ordering rule of that kernel).
+ * INT8 MV kernel).  M == 1: one kernel quantizes the row and runs the
+ * matrix-vector product with the fused dequant.  2 <= M <= 8, per channel,
+ * with the codes of the rows (padded to 2, 4 or 8) within 64 KB: one kernel
+ * quantizes the rows and runs the few-row product on the same weight
+ * stream.  In both, the workspace is checked but not written (see w8a8_mv
+ * for the ordering rule of those kernels).  Otherwise: quantize x per token
+ * into the workspace (quantize_act_per_token_h), then the GEMM
+ * (w8a8_gemm_h) with the fused dequant.  Same quantization rule everywhere.
  *   x        fp16 [M, K]
  *   Wq       int8 [N, K] (wbits 8) or packed uint8 [N, K/2] (wbits 4)
  *   scale_w  fp32 [N, G] (wbits 4 requires group_size 0)

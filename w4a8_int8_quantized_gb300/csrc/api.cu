@@ -257,12 +257,10 @@ int linear(const w8a8_half *x, const void *Wq, const float *scale_w, int M,
                             wbits, reinterpret_cast<__half *>(y), s);
   }
   if (skinny_supported(M, K, group_size)) {
-    // a few rows: INT8 codes into the workspace, then the weight stream of
-    // the matrix-vector kernel (launched early; it waits for the codes)
-    int8_t *xq = static_cast<int8_t *>(workspace);
-    W8A8_TRY(launch_row_quant_act(reinterpret_cast<const __half *>(x), M, K, group_size, xq, sa,
-                                  s));
-    return launch_skinny(xq, sa, Wq, scale_w, M, N, K, wbits, reinterpret_cast<__half *>(y), s);
+    // a few rows: one kernel quantizes them and streams the weights (the
+    // workspace is checked but not written)
+    return launch_linear_rows(reinterpret_cast<const __half *>(x), Wq, scale_w, M, N, K, wbits,
+                              reinterpret_cast<__half *>(y), s);
   }
   __half *xq_h = static_cast<__half *>(workspace);
   W8A8_TRY(launch_row_quant_half(reinterpret_cast<const __half *>(x), M, K, group_size, xq_h,

@@ -90,10 +90,10 @@ bool skinny_supported(int M, int K, int group_size);
 int launch_skinny(const int8_t *xq, const float *sa, const void *W, const float *sw, int M, int N,
                   int K, int wbits, __half *y, cudaStream_t s);
 
-// Activation quantization to INT8 codes that lets the next kernel on the
-// stream launch early (it must wait for this grid before reading the codes).
-int launch_row_quant_act(const __half *x, int R, int K, int group_size, int8_t *q, float *scale,
-                         cudaStream_t s);
+// The whole layer for 2 <= M <= kSkinnyMaxM fp16 rows (skinny_supported):
+// quantization fused into the few-row kernel.
+int launch_linear_rows(const __half *x, const void *W, const float *sw, int M, int N, int K,
+                       int wbits, __half *y, cudaStream_t s);
 
 // Row quantization writing the INT8 codes as fp16 values.
 int launch_row_quant_half(const __half *x, int R, int K, int group_size, __half *qh,

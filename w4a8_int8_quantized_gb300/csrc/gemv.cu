@@ -140,15 +140,6 @@ __device__ __forceinline__ bool wait_copy(uint32_t bar, long long limit) {
   return true;
 }
 
-// acc + the dot product of 16 INT8 pairs
-__device__ __forceinline__ int dot16acc(const uint4 &w, const uint4 &a, int acc) {
-  acc = __dp4a(static_cast<int>(w.x), static_cast<int>(a.x), acc);
-  acc = __dp4a(static_cast<int>(w.y), static_cast<int>(a.y), acc);
-  acc = __dp4a(static_cast<int>(w.z), static_cast<int>(a.z), acc);
-  acc = __dp4a(static_cast<int>(w.w), static_cast<int>(a.w), acc);
-  return acc;
-}
-
 __device__ __forceinline__ int dot16(const uint4 &w, const uint4 &a) {
   int acc = __dp4a(static_cast<int>(w.x), static_cast<int>(a.x), 0);
   acc = __dp4a(static_cast<int>(w.y), static_cast<int>(a.y), acc);
@@ -210,7 +201,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) mv_kernel(
     const void *__restrict__ xin, const float *__restrict__ sa_in,
     const uint8_t *__restrict__ W, const float *__restrict__ sw, int M, int N, int K, int gs,
     __half *__restrict__ y, unsigned int *err) {
-  static_assert(!(PERGROUP && MR > 1) && !(FUSED && MR > 1), "per group and fused: one row");
+  static_assert(!(PERGROUP && MR > 1), "per group: one row");
+  // the fused single row is staged by one bulk copy; fused rows of a
+  // few-row product are read by one warp each
+  constexpr bool STAGED = FUSED && MR == 1;
   constexpr int U = pipe_depth<MR>();
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int red_i[kWarps][MR];
@@ -229,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) mv_kernel(
   const int nsteps = (se - sb + 31) >> 5;
   const int nseg = se - sb;
   const uint4 *wg = reinterpret_cast<const uint4 *>(W + r0 * row_bytes) + sb + lane;
-  const __half *xrow = reinterpret_cast<const __half *>(smem);  // fused: the staged fp16 row
-  int8_t *xs = reinterpret_cast<int8_t *>(smem + (FUSED ? 2 * K : 0));
+  const __half *xrow = reinterpret_cast<const __half *>(smem);  // staged fp16 row
+  int8_t *xs = reinterpret_cast<int8_t *>(smem + (STAGED ? 2 * K : 0));
   float *ss = reinterpret_cast<float *>(xs + static_cast<size_t>(MR) * K);
   int *acc = reinterpret_cast<int *>(ss + MR * G);
   float *sws = reinterpret_cast<float *>(acc + rows * G * (PERGROUP ? 1 : MR));
@@ -240,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) mv_kernel(
     return 32 * j + lane < nseg ? ldg_stream(wg + 32 * j) : make_uint4(0, 0, 0, 0);
   };
 
-  if (FUSED) {
+  if (STAGED) {
     if (tid == 0) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&xbar)));
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -261,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) mv_kernel(
   }
   // everything below may read what the previous kernel on the stream wrote
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (FUSED && tid == 0) {
+  if (STAGED && tid == 0) {
     // the fp16 row by one bulk copy: it does not queue behind the weight
     // loads this SM has in flight, as per-thread loads of x would
     const uint32_t bytes = 2u * static_cast<uint32_t>(K);
@@ -285,7 +279,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) mv_kernel(
   int asum[MR];  // W4: this thread's share of sum_k q_mk
 #pragma unroll
   for (int m = 0; m < MR; ++m) asum[m] = 0;
-  if (FUSED) {
+  if (FUSED && !STAGED) {
+    // each warp quantizes whole rows m = warp, warp + 8, ... (one scale per
+    // row: the absmax is a warp reduction, no block barrier); rows m >= M
+    // get zero codes and scale 0
+    const int nvec = K >> 3;
+    for (int m = warp; m < MR; m += kWarps) {
+      const uint4 *xr = xv + static_cast<long>(m) * nvec;
+      float amax = 0.f;
+      if (m < M)
+        for (int v = lane; v < nvec; v += 32) amax = fmaxf(amax, absmax8(__ldg(xr + v)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float sm_ = __fdiv_rn(amax, 127.f);
+      const float rcp = amax == 0.f ? 0.f : __frcp_rn(sm_);
+      if (lane == 0) ss[m] = m < M ? sm_ : 0.f;
+      int as = 0;
+      for (int v = lane; v < nvec; v += 32) {
+        float q[8];
+        quant_vec8(m < M ? __ldg(xr + v) : make_uint4(0, 0, 0, 0), sm_, rcp, q);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) as += __float2int_rn(q[j]);
+        reinterpret_cast<uint2 *>(xs + static_cast<long>(m) * K)[v] = pack_i8x8(q);
+      }
+#pragma unroll
+      for (int mm = 0; mm < MR; ++mm)
+        if (mm == m) asum[mm] += as;
+    }
+  } else if (FUSED) {
     if (!wait_copy(smem_u32(&xbar), kCopyWaitCycles)) {
       // record the failure; still let the copy land before going on
       if (err != nullptr) atomicCAS(err, 0u, static_cast<unsigned>(kDevErrRowCopy));
@@ -547,7 +568,7 @@ int launch_mv_t(const void *xin, const float *sa, const void *W, const float *sw
     std::lock_guard<std::mutex> lock(mu);
     if (!attr_set[dev]) {
       const size_t most = MR == 1 ? mv_state_bytes(kMaxK, kMaxK / 64, 0, PERGROUP, 1, FUSED)
-                                  : static_cast<size_t>(kSkinnyMaxCodeBytes) + 4 * MR;
+                                  : static_cast<size_t>(kSkinnyMaxCodeBytes) + 4 * MR;  // not staged
       if (cudaFuncSetAttribute(mv_kernel<WBITS, PERGROUP, FUSED, MR, WALK>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(most + kAccBytesMax)) != cudaSuccess)
@@ -566,7 +587,7 @@ int launch_mv_t(const void *xin, const float *sa, const void *W, const float *sw
   if (grid < need) grid = need;
   if (grid > N) grid = N;
   const int rows_max = static_cast<int>((N + grid - 1) / grid);
-  const size_t smem = mv_state_bytes(K, G, rows_max, PERGROUP, MR, FUSED);
+  const size_t smem = mv_state_bytes(K, G, rows_max, PERGROUP, MR, FUSED && MR == 1);
   unsigned int *err = device_error_word();
   if (err == nullptr) return W8A8_ERR_CUDA;
 
@@ -604,6 +625,12 @@ template <int WBITS, int MR>
 int launch_rows(const int8_t *xq, const float *sa, const void *W, const float *sw, int M, int N,
                 int K, __half *y, cudaStream_t s) {
   return launch_mv<WBITS, false, false, MR>(xq, sa, W, sw, M, N, K, 0, y, s);
+}
+
+template <int WBITS, int MR>
+int launch_rows_fused(const __half *x, const void *W, const float *sw, int M, int N, int K,
+                      __half *y, cudaStream_t s) {
+  return launch_mv<WBITS, false, true, MR>(x, nullptr, W, sw, M, N, K, 0, y, s);
 }
 
 }  // namespace
@@ -648,6 +675,21 @@ int launch_skinny(const int8_t *xq, const float *sa, const void *W, const float 
     default:
       return wbits == 4 ? launch_rows<4, 8>(xq, sa, W, sw, M, N, K, y, s)
                         : launch_rows<8, 8>(xq, sa, W, sw, M, N, K, y, s);
+  }
+}
+
+int launch_linear_rows(const __half *x, const void *W, const float *sw, int M, int N, int K,
+                       int wbits, __half *y, cudaStream_t s) {
+  switch (skinny_rows(M)) {
+    case 2:
+      return wbits == 4 ? launch_rows_fused<4, 2>(x, W, sw, M, N, K, y, s)
+                        : launch_rows_fused<8, 2>(x, W, sw, M, N, K, y, s);
+    case 4:
+      return wbits == 4 ? launch_rows_fused<4, 4>(x, W, sw, M, N, K, y, s)
+                        : launch_rows_fused<8, 4>(x, W, sw, M, N, K, y, s);
+    default:
+      return wbits == 4 ? launch_rows_fused<4, 8>(x, W, sw, M, N, K, y, s)
+                        : launch_rows_fused<8, 8>(x, W, sw, M, N, K, y, s);
   }
 }
 

@@ -29,9 +29,7 @@
 namespace w8a8 {
 namespace {
 
-// kOutInt8Act: INT8 codes of activations for a dependent that waits for
-// this grid (the few-row product), so the dependent may launch early.
-enum OutMode { kOutInt8 = 0, kOutHalf = 1, kOutInt4 = 2, kOutInt8Act = 3 };
+enum OutMode { kOutInt8 = 0, kOutHalf = 1, kOutInt4 = 2 };
 
 // Resident CTAs per SM to aim for: the loads in flight (the only latency
 // hiding this one-pass kernel has) scale with it.  Five CTAs (<= 51
@@ -49,7 +47,7 @@ __global__ void __launch_bounds__(256, quant_min_blocks<V>()) row_quant_kernel(
   // activation codes for the GEMM: let it launch now and run its prologue
   // while this grid finishes (it waits for this grid before reading any
   // input); the weight quantizers (other modes) never start dependents early
-  if (MODE == kOutHalf || MODE == kOutInt8Act) asm volatile("griddepcontrol.launch_dependents;");
+  if (MODE == kOutHalf) asm volatile("griddepcontrol.launch_dependents;");
   __shared__ float red[8];
   const int nvec = K >> 3;
   const int t = threadIdx.x % T;
@@ -117,7 +115,7 @@ __global__ void __launch_bounds__(256, quant_min_blocks<V>()) row_quant_kernel(
     // a zero row or group has s = 0 and rcp = 0: t = 0 and every code is 0
     float q[8];
     quant_vec8(v[i], s, rcp, q);
-    if (MODE == kOutInt8 || MODE == kOutInt8Act) {
+    if (MODE == kOutInt8) {
       reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + r * K)[vi] = pack_i8x8(q);
     } else if (MODE == kOutHalf) {
       // integral codes of magnitude <= 127 are fp16 values exactly; + 0
@@ -181,12 +179,6 @@ int launch_row_quant(const __half *x, int R, int K, int group_size, int qmax,
   if (packed != nullptr)
     return launch_mode<kOutInt4>(x, R, K, group_size, qmax, packed, scale, s);
   return launch_mode<kOutInt8>(x, R, K, group_size, qmax, q, scale, s);
-}
-
-int launch_row_quant_act(const __half *x, int R, int K, int group_size, int8_t *q, float *scale,
-                         cudaStream_t s) {
-  if (R == 0) return W8A8_OK;
-  return launch_mode<kOutInt8Act>(x, R, K, group_size, 127, q, scale, s);
 }
 
 int launch_row_quant_half(const __half *x, int R, int K, int group_size, __half *qh,
