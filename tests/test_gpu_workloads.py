@@ -95,7 +95,7 @@ def test_per_group(gs):
     M = cfg["Ms"][0]
     x = synth.activations(M, cfg["K"], seed=0, **cfg["act"])
     W = synth.weights(cfg["N"], cfg["K"], seed=0)
-    run_layer(x, W, gs=gs)
+    run_layer(x, W, gs=gs, exact=False)
 
 
 @pytest.mark.parametrize("M", synth.WORKLOADS["w4a8"]["Ms"])

@@ -310,7 +310,7 @@ __device__ __forceinline__ uint4 i4x8_to_h(uint32_t w) {
 }
 
 // Two scale products s_i * w with one paired fp32 multiply (each half an
-// IEEE multiply rounded to nearest; nothing follows it that could fuse).
+// IEEE multiply rounded to nearest).
 __device__ __forceinline__ void mul2(float s0, float s1, float w, float &p0, float &p1) {
   asm("{\n.reg .b64 a, b, c;\n"
       "mov.b64 a, {%2, %3};\n"
@@ -319,6 +319,20 @@ __device__ __forceinline__ void mul2(float s0, float s1, float w, float &p0, flo
       "mov.b64 {%0, %1}, c;\n}\n"
       : "=f"(p0), "=f"(p1)
       : "f"(s0), "f"(s1), "f"(w));
+}
+
+// f_i = fma(v_i, s_i, f_i) for two lanes with one paired fused multiply-add
+// (f and v are fp32 bit patterns held in integer registers).
+__device__ __forceinline__ void fma2(uint32_t &f0, uint32_t &f1, uint32_t v0, uint32_t v1,
+                                     float s0, float s1) {
+  asm("{\n.reg .b64 a, b, c, d;\n"
+      "mov.b64 a, {%2, %3};\n"
+      "mov.b64 b, {%4, %5};\n"
+      "mov.b64 c, {%0, %1};\n"
+      "fma.rn.f32x2 d, a, b, c;\n"
+      "mov.b64 {%0, %1}, d;\n}\n"
+      : "+r"(f0), "+r"(f1)
+      : "r"(v0), "r"(v1), "f"(s0), "f"(s1));
 }
 
 // Converts sub-tile `sub` (codes 64 sub .. 64 sub + 63 of each of ROWS rows)
@@ -415,12 +429,14 @@ __device__ __forceinline__ void tmem_wait_ld32(uint32_t (&v)[32]) {
 // 16 columns at a time, measured slower per group).  Modes:
 //   exact per channel: each chunk is converted to int32 (exact) and summed
 //     in integer; y = fp16(float(sum) * (s_a * s_w));
-//   exact per group: each group is rescaled in fp32 and accumulated in
-//     ascending order, f += acc_g * (s_a,g * s_w,g) (the scale products two
-//     at a time by a paired multiply; the oracle's rounding sequence);
-//     y = fp16(f);
+//   per group: each group's exact partial is rescaled and accumulated in
+//     ascending order, f = fma(acc_g, s_a,g * s_w,g, f), two lanes per
+//     instruction (paired multiply for the scale products, paired fused
+//     multiply-add); the fused form skips the rounding of each product
+//     (at most half an ulp of acc_g * s per group), far inside the fp16
+//     tolerance, and halves the drain's instructions; y = fp16(f);
 //   weight-only (WONLY, fp16 activations): one float accumulation over K,
-//     y = fp16(acc * s_w), or per group f += acc_g * s_w,g.
+//     y = fp16(acc * s_w), or per group f = fma(acc_g, s_w,g, f).
 template <bool PERGROUP, bool WONLY, int BT>
 __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, uint32_t base,
                                               uint8_t *sm, int off_sa, int warp, int lane,
@@ -511,16 +527,12 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
                 sc[0] = sc[1] = sc[2] = sc[3] = sw_g;
               } else {
                 const float4 s4 = lds_f32x4(sas + (gb * BT + half * CPT + j * 32 + i4 * 4) * 4);
-                mul2(s4.x, s4.y, sw_g, sc[0], sc[1]);  // (s_a * s_w) first, as in the dequant rule
+                mul2(s4.x, s4.y, sw_g, sc[0], sc[1]);  // s_a * s_w first, as in the dequant rule
                 mul2(s4.z, s4.w, sw_g, sc[2], sc[3]);
               }
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int idx = j * 32 + i4 * 4 + e;
-                acc[idx] = __float_as_uint(__fadd_rn(
-                    __uint_as_float(acc[idx]), __fmul_rn(__uint_as_float(v[i4 * 4 + e]), sc[e])));
-                asm volatile("" : "+r"(acc[idx]));  // before the next scale load
-              }
+              const int idx = j * 32 + i4 * 4;
+              fma2(acc[idx], acc[idx + 1], v[i4 * 4], v[i4 * 4 + 1], sc[0], sc[1]);
+              fma2(acc[idx + 2], acc[idx + 3], v[i4 * 4 + 2], v[i4 * 4 + 3], sc[2], sc[3]);
             }
           } else if (n < p.N) {
             // export of the exact group partials; sequential addresses
