@@ -118,16 +118,8 @@ __global__ void __launch_bounds__(256, quant_min_blocks<V>()) row_quant_kernel(
     if (MODE == kOutInt8) {
       reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + r * K)[vi] = pack_i8x8(q);
     } else if (MODE == kOutHalf) {
-      // integral codes of magnitude <= 127 are fp16 values exactly; + 0
-      // turns a -0 code into +0, the fp16 value of the integer 0
-      uint32_t w[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __half2 hh = __floats2half2_rn(q[2 * j] + 0.f, q[2 * j + 1] + 0.f);
-        w[j] = *reinterpret_cast<const uint32_t *>(&hh);
-      }
-      reinterpret_cast<uint4 *>(static_cast<__half *>(out) + r * K)[vi] =
-          make_uint4(w[0], w[1], w[2], w[3]);
+      // integral codes of magnitude <= 127 are fp16 values exactly
+      reinterpret_cast<uint4 *>(static_cast<__half *>(out) + r * K)[vi] = pack_h8(q);
     } else {
       uint32_t w = 0;
 #pragma unroll
