@@ -301,9 +301,11 @@ def run_reference(args):
 
 # -------------------------------------------------------------- GPU path --
 
-def measure_workloads(w8, torch, device, flush_l2, l2_bytes, tflops_peak, hbm_peak, reps=10):
+def measure_workloads(w8, torch, device, flush_l2, l2_bytes, tflops_peak, hbm_peak, reps=20):
     """Every other workload of the layer, timed once per case with CUDA events
-    (median of `reps`): the 512 x 512 per-channel layer, per group gs 128 /
+    (mean of `reps`; event timestamps on this GPU advance in steps of about
+    2 us, so a median of single calls sits on a step and a mean over the
+    jittered samples does not): the 512 x 512 per-channel layer, per group gs 128 /
     64, W4A8 at M = 2048 and M = 1, and the linear layers of an 8B-class
     decoder block at M = 4516 and M = 1.  GEMM-type calls run after an L2
     flush; decode calls run back to back over weight copies larger than L2
@@ -323,7 +325,7 @@ def measure_workloads(w8, torch, device, flush_l2, l2_bytes, tflops_peak, hbm_pe
             e1.record(stream)
             torch.cuda.synchronize()
             ts.append(e0.elapsed_time(e1) / inner)
-        return statistics.median(ts)
+        return statistics.fmean(ts)
 
     def dev(a):
         return torch.from_numpy(a).to(device)
