@@ -60,7 +60,7 @@ UNIT = "TOPS"
 # section "cider의 성능 측정 결과"): the same metric as a whole-sweep rate.
 PAGES_MS = {1: 0.27, 128: 0.34, 1024: 1.23, 4096: 4.41, 8192: 8.71}
 PAGES_TOPS = sum(2.0 * m * N_OUT * K_IN for m in MS) / (sum(PAGES_MS.values()) * 1e-3) / 1e12
-E2E_CHUNK_ROWS = 1024  # rows per pipelined chunk of the e2e measurement
+E2E_CHUNK_ROWS = 512  # rows per pipelined chunk of the e2e measurement
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -595,7 +595,7 @@ def run_ours(args):
         if record is not None:
             record.append(evs)
 
-    # e2e: from M = 2048 on, the rows go in chunks of E2E_CHUNK_ROWS, the
+    # e2e: from M = 2 chunk_rows on, the rows go in chunks of chunk_rows, the
     # host->device copy of chunk i+1, the layer on chunk i and the
     # device->host copy of chunk i-1 overlapping on three streams (the copy
     # engines of the two directions and the SMs work at once); smaller M runs
@@ -604,8 +604,10 @@ def run_ours(args):
     s_h2d, s_comp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     comp_ptr = ctypes.c_void_p(s_comp.cuda_stream)
 
+    chunk_rows = args.e2e_chunk_rows
+
     def e2e_chunks(m):
-        return m // E2E_CHUNK_ROWS if m >= 2 * E2E_CHUNK_ROWS else 1
+        return m // chunk_rows if m >= 2 * chunk_rows else 1
 
     def linear_rows(m, r0, r1, sptr):
         b = bufs[m]
@@ -797,8 +799,8 @@ def run_ours(args):
                     "h2d_bytes_per_step": sum(m * K_IN * 2 for m in MS),
                     "d2h_bytes_per_step": sum(m * N_OUT * 2 for m in MS),
                     "method": f"C ABI linear() per M from pinned host buffers, L2 flushed "
-                              f"before each M; M >= {2 * E2E_CHUNK_ROWS} in chunks of "
-                              f"{E2E_CHUNK_ROWS} rows with copy-in, layer and copy-out "
+                              f"before each M; M >= {2 * chunk_rows} in chunks of "
+                              f"{chunk_rows} rows with copy-in, layer and copy-out "
                               f"overlapped on three streams",
                     "outputs_equal_single_stream_linear": e2e_mismatch == 0,
                     "mismatched_outputs": e2e_mismatch},
@@ -881,6 +883,8 @@ def main():
     ap.add_argument("--only", choices=["quant", "quant_i8", "gemm", "gemm_i8", "w4a8", "linear",
                                        "linear4"],
                     help="run one kernel of the path on one shape (for profilers)")
+    ap.add_argument("--e2e-chunk-rows", type=int, default=E2E_CHUNK_ROWS,
+                    help="rows per pipelined chunk of the end-to-end measurement")
     ap.add_argument("--m", type=int, default=8192)
     ap.add_argument("--n", type=int, default=N_OUT)
     ap.add_argument("--k", type=int, default=K_IN)
