@@ -79,11 +79,16 @@ constexpr long long kTimeoutCycles = 4000000000LL;
 // time (one MMA commit per REL stages).
 //
 // Every stage costs the same hand-offs between the roles (staging copy ->
-// converters -> MMA -> release), about 600 cycles of barrier round trips
-// measured with no data moved and no MMA issued, so KS = 2 (two K blocks
-// behind one hand-off, two stages of 96 KB) halves that cost per FLOP.  It
-// needs the full 227 KB, with no room for aligning the dynamic shared
-// memory by hand: the kernel checks that its base is 1 KB aligned instead.
+// converters -> MMA -> release), so KS = 2 (two K blocks behind one
+// hand-off, two stages of 96 KB) halves that cost per FLOP; single-K-block
+// stages, even four of them, measured slower.  What bounds the two-stage
+// ring (clock64 trace of one CTA at M = 8192): a stage's activation copy is
+// issued ~675 cycles after the last MMA of the stage whose slot it refills
+// (MMA completion, commit, wake-up) and lands ~2000 cycles later, against
+// ~1000 cycles of MMAs in the other stage, so the tensor pipe waits ~40 % of
+// the time.  The plan needs the full 227 KB, with no room for aligning the
+// dynamic shared memory by hand: the kernel checks that its base is 1 KB
+// aligned instead.
 template <bool XH, int BT, int KS>
 struct Plan {
   static constexpr int KB = BK * KS;                // K per stage
