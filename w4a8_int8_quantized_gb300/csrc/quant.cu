@@ -23,6 +23,8 @@
 // fp16 integer exactly), or INT4 codes packed two per byte.
 //
 // Rounding: see quant_rule.cuh.
+#include <mutex>
+
 #include "common.cuh"
 #include "quant_rule.cuh"
 
@@ -129,6 +131,90 @@ __global__ void __launch_bounds__(256, quant_min_blocks<V>()) row_quant_kernel(
   }
 }
 
+// Per-token fp16-code quantization as a persistent grid: team g of T
+// threads owns rows g, g + nteams, ... and loads its next row while it
+// quantizes the current one, so every SM keeps two rows per team in flight
+// and no CTA is launched per row.  The team's absmax goes through a named
+// barrier of its own T threads (teams leave the loop independently), with
+// the shared partials double-buffered by row parity.
+template <int V>
+__global__ void __launch_bounds__(256, V <= 2 ? 4 : 3) row_quant_half_rows(const uint4 *__restrict__ x, long R,
+                                                             int K, int T, __half *__restrict__ out,
+                                                             float *__restrict__ scale) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  __shared__ float red[2][8];
+  const int nvec = K >> 3;
+  const int t = threadIdx.x % T, team = threadIdx.x / T, teams = blockDim.x / T;
+  const int warp = threadIdx.x >> 5, wpt = T >> 5;
+  const long nteams = static_cast<long>(gridDim.x) * teams;
+  long r = static_cast<long>(blockIdx.x) * teams + team;
+  auto load = [&](long row, uint4 (&v)[V]) {
+    const uint4 *xr = x + row * nvec;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = i * T + t;
+      v[i] = (row < R && vi < nvec) ? __ldcs(xr + vi) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 cur[V], nxt[V];
+  load(r, cur);
+  for (int it = 0; r < R; r += nteams, ++it) {
+    load(r + nteams, nxt);
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) amax = fmaxf(amax, absmax8(cur[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (T > 32) {
+      if ((threadIdx.x & 31) == 0) red[it & 1][warp] = amax;
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(T) : "memory");
+      amax = 0.f;
+      for (int w = 0; w < wpt; ++w) amax = fmaxf(amax, red[it & 1][team * wpt + w]);
+    }
+    const float s_row = __fdiv_rn(amax, 127.f);
+    const float rcp_row = amax == 0.f ? 0.f : __frcp_rn(s_row);
+    if (t == 0) scale[r] = s_row;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int vi = i * T + t;
+      if (vi < nvec) {
+        float q[8];
+        quant_vec8(cur[i], s_row, rcp_row, q);
+        reinterpret_cast<uint4 *>(out + r * K)[vi] = pack_h8(q);
+      }
+      cur[i] = nxt[i];
+    }
+  }
+}
+
+template <int V>
+int launch_rows_half(const __half *x, long R, int K, int T, __half *out, float *scale,
+                     cudaStream_t s) {
+  static int blocks[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return W8A8_ERR_CUDA;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (blocks[dev] == 0) {
+      int nsm = 0, occ = 0;
+      if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, row_quant_half_rows<V>, 256, 0) !=
+              cudaSuccess || occ < 1)
+        return W8A8_ERR_CUDA;
+      blocks[dev] = nsm * occ;
+    }
+    per_sm = blocks[dev];
+  }
+  const int teams = 256 / T;
+  const long need = (R + teams - 1) / teams;
+  const long grid = need < per_sm ? need : per_sm;
+  row_quant_half_rows<V><<<static_cast<unsigned>(grid), 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), R, K, T, out, scale);
+  return launch_status();
+}
+
 template <int V, int MODE>
 int launch_v(const __half *x, long R, int K, int gs, int qmax, int T, void *out,
              float *scale, cudaStream_t s) {
@@ -149,6 +235,15 @@ int launch_mode(const __half *x, int R, int K, int group_size, int qmax, void *o
   int T = 32;
   while (T < 256 && (nvec + T - 1) / T > 4) T <<= 1;
   const int V = (nvec + T - 1) / T;
+  if (MODE == kOutHalf && group_size == 0 && V <= 4) {
+    __half *qh = static_cast<__half *>(out);
+    switch (V) {
+      case 1: return launch_rows_half<1>(x, R, K, T, qh, scale, s);
+      case 2: return launch_rows_half<2>(x, R, K, T, qh, scale, s);
+      case 3: return launch_rows_half<3>(x, R, K, T, qh, scale, s);
+      default: return launch_rows_half<4>(x, R, K, T, qh, scale, s);
+    }
+  }
   switch (V) {
 #define W8A8_CASE(n) \
   case n:            \
