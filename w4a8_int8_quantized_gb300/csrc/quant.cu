@@ -131,19 +131,22 @@ __global__ void __launch_bounds__(256, quant_min_blocks<V>()) row_quant_kernel(
   }
 }
 
-// Per-token fp16-code quantization as a persistent grid: team g of T
+// fp16-code activation quantization as a persistent grid: team g of T
 // threads owns rows g, g + nteams, ... and loads its next row while it
 // quantizes the current one, so every SM keeps two rows per team in flight
-// and no CTA is launched per row.  The team's absmax goes through a named
-// barrier of its own T threads (teams leave the loop independently), with
-// the shared partials double-buffered by row parity.
-template <int V>
+// and no CTA is launched per row.  Per token, the team's absmax goes through
+// a named barrier of its own T threads (teams leave the loop independently),
+// with the shared partials double-buffered by row parity; per group (gs > 0)
+// a group is gs / 8 consecutive lanes of one warp, reduced with shuffles.
+template <int V, bool PG>
 __global__ void __launch_bounds__(256, V <= 2 ? 4 : 3) row_quant_half_rows(const uint4 *__restrict__ x, long R,
-                                                             int K, int T, __half *__restrict__ out,
+                                                             int K, int gs, int T,
+                                                             __half *__restrict__ out,
                                                              float *__restrict__ scale) {
   asm volatile("griddepcontrol.launch_dependents;");
   __shared__ float red[2][8];
   const int nvec = K >> 3;
+  const int G = gs == 0 ? 1 : K / gs;
   const int t = threadIdx.x % T, team = threadIdx.x / T, teams = blockDim.x / T;
   const int warp = threadIdx.x >> 5, wpt = T >> 5;
   const long nteams = static_cast<long>(gridDim.x) * teams;
@@ -160,26 +163,44 @@ __global__ void __launch_bounds__(256, V <= 2 ? 4 : 3) row_quant_half_rows(const
   load(r, cur);
   for (int it = 0; r < R; r += nteams, ++it) {
     load(r + nteams, nxt);
+    float vmax[V];
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < V; ++i) amax = fmaxf(amax, absmax8(cur[i]));
+    for (int i = 0; i < V; ++i) {
+      vmax[i] = absmax8(cur[i]);
+      amax = fmaxf(amax, vmax[i]);
+    }
+    if (!PG) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (T > 32) {
-      if ((threadIdx.x & 31) == 0) red[it & 1][warp] = amax;
-      asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(T) : "memory");
-      amax = 0.f;
-      for (int w = 0; w < wpt; ++w) amax = fmaxf(amax, red[it & 1][team * wpt + w]);
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (T > 32) {
+        if ((threadIdx.x & 31) == 0) red[it & 1][warp] = amax;
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(T) : "memory");
+        amax = 0.f;
+        for (int w = 0; w < wpt; ++w) amax = fmaxf(amax, red[it & 1][team * wpt + w]);
+      }
+    } else {
+      const int width = gs >> 3;
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        for (int o = width >> 1; o > 0; o >>= 1)
+          vmax[i] = fmaxf(vmax[i], __shfl_xor_sync(0xffffffffu, vmax[i], o));
     }
     const float s_row = __fdiv_rn(amax, 127.f);
     const float rcp_row = amax == 0.f ? 0.f : __frcp_rn(s_row);
-    if (t == 0) scale[r] = s_row;
+    if (!PG && t == 0) scale[r] = s_row;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int vi = i * T + t;
       if (vi < nvec) {
+        float sc = s_row, rc = rcp_row;
+        if (PG) {
+          sc = __fdiv_rn(vmax[i], 127.f);
+          rc = vmax[i] == 0.f ? 0.f : __frcp_rn(sc);
+          if ((t & ((gs >> 3) - 1)) == 0) scale[r * G + (vi << 3) / gs] = sc;
+        }
         float q[8];
-        quant_vec8(cur[i], s_row, rcp_row, q);
+        quant_vec8(cur[i], sc, rc, q);
         reinterpret_cast<uint4 *>(out + r * K)[vi] = pack_h8(q);
       }
       cur[i] = nxt[i];
@@ -187,8 +208,8 @@ __global__ void __launch_bounds__(256, V <= 2 ? 4 : 3) row_quant_half_rows(const
   }
 }
 
-template <int V>
-int launch_rows_half(const __half *x, long R, int K, int T, __half *out, float *scale,
+template <int V, bool PG>
+int launch_rows_half(const __half *x, long R, int K, int gs, int T, __half *out, float *scale,
                      cudaStream_t s) {
   static int blocks[64] = {};
   static std::mutex mu;
@@ -200,7 +221,7 @@ int launch_rows_half(const __half *x, long R, int K, int T, __half *out, float *
     if (blocks[dev] == 0) {
       int nsm = 0, occ = 0;
       if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, row_quant_half_rows<V>, 256, 0) !=
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, row_quant_half_rows<V, PG>, 256, 0) !=
               cudaSuccess || occ < 1)
         return W8A8_ERR_CUDA;
       blocks[dev] = nsm * occ;
@@ -210,8 +231,8 @@ int launch_rows_half(const __half *x, long R, int K, int T, __half *out, float *
   const int teams = 256 / T;
   const long need = (R + teams - 1) / teams;
   const long grid = need < per_sm ? need : per_sm;
-  row_quant_half_rows<V><<<static_cast<unsigned>(grid), 256, 0, s>>>(
-      reinterpret_cast<const uint4 *>(x), R, K, T, out, scale);
+  row_quant_half_rows<V, PG><<<static_cast<unsigned>(grid), 256, 0, s>>>(
+      reinterpret_cast<const uint4 *>(x), R, K, gs, T, out, scale);
   return launch_status();
 }
 
@@ -235,13 +256,21 @@ int launch_mode(const __half *x, int R, int K, int group_size, int qmax, void *o
   int T = 32;
   while (T < 256 && (nvec + T - 1) / T > 4) T <<= 1;
   const int V = (nvec + T - 1) / T;
-  if (MODE == kOutHalf && group_size == 0 && V <= 4) {
+  if (MODE == kOutHalf && V <= 4) {
     __half *qh = static_cast<__half *>(out);
+    if (group_size != 0) {
+      switch (V) {
+        case 1: return launch_rows_half<1, true>(x, R, K, group_size, T, qh, scale, s);
+        case 2: return launch_rows_half<2, true>(x, R, K, group_size, T, qh, scale, s);
+        case 3: return launch_rows_half<3, true>(x, R, K, group_size, T, qh, scale, s);
+        default: return launch_rows_half<4, true>(x, R, K, group_size, T, qh, scale, s);
+      }
+    }
     switch (V) {
-      case 1: return launch_rows_half<1>(x, R, K, T, qh, scale, s);
-      case 2: return launch_rows_half<2>(x, R, K, T, qh, scale, s);
-      case 3: return launch_rows_half<3>(x, R, K, T, qh, scale, s);
-      default: return launch_rows_half<4>(x, R, K, T, qh, scale, s);
+      case 1: return launch_rows_half<1, false>(x, R, K, 0, T, qh, scale, s);
+      case 2: return launch_rows_half<2, false>(x, R, K, 0, T, qh, scale, s);
+      case 3: return launch_rows_half<3, false>(x, R, K, 0, T, qh, scale, s);
+      default: return launch_rows_half<4, false>(x, R, K, 0, T, qh, scale, s);
     }
   }
   switch (V) {
