@@ -122,9 +122,14 @@ def test_act_quant_exhaustive_fp16(amax):
     np.testing.assert_array_equal(host(sh), rs)
 
 
-@pytest.mark.parametrize("M,K,gs", [(3, 48, 0), (130, 2560, 128), (257, 4096, 64), (5, 14336, 0)])
+@pytest.mark.parametrize("M,K,gs", [(3, 48, 0), (130, 2560, 128), (257, 4096, 64), (5, 14336, 0),
+                                   (3001, 2560, 0), (2999, 4096, 128), (1801, 1024, 64),
+                                   (4099, 256, 0), (2500, 8192, 0)])
 def test_act_quant_half_codes(M, K, gs):
-    """quantize_act_per_token_h writes exactly the INT8 codes, as fp16."""
+    """quantize_act_per_token_h writes exactly the INT8 codes, as fp16.  The
+    larger M make every row team of the persistent kernel take several rows
+    (with its next row loaded while the current one is quantized), with a
+    ragged last round; K from 256 (one vector per thread) to 8192 (four)."""
     x = act(M, K, seed=K + 1, zero_rows=(0,), n_outliers=3, outlier_scale=40.0)
     xh, sa = w8.quantize_act_per_token_h(dev(x), gs)
     rq, rs = oracle.quantize_act_per_token(x, gs)
