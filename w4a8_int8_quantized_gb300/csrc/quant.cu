@@ -9,7 +9,11 @@
 // weights packed two per uint8 for W4A8).
 //
 // Design (HBM-bound, one streaming pass): a team of T threads (32 to 256,
-// so that each thread caches at most 4 vectors where K allows) owns one row.  Each thread
+// so that each thread caches at most 4 vectors where K allows) owns a row.
+// Activation codes (INT8 or fp16, K <= 8192) and INT8 weights run on a
+// persistent grid whose teams take row after row, each loading its next row
+// while it quantizes the current one (row_quant_rows); INT4 weights and
+// longer rows launch one team per row (row_quant_kernel).  Each thread
 // loads its V 16-byte vectors (8 fp16 each) once into registers, the team
 // reduces absmax with warp shuffles (and shared memory when T > 32), and the
 // same registers are quantized and stored.  Vector i of thread t covers
@@ -131,19 +135,23 @@ __global__ void __launch_bounds__(256, quant_min_blocks<V>()) row_quant_kernel(
   }
 }
 
-// fp16-code activation quantization as a persistent grid: team g of T
+// Activation quantization (INT8 codes, or the same codes as fp16 values) as
+// a persistent grid: team g of T
 // threads owns rows g, g + nteams, ... and loads its next row while it
 // quantizes the current one, so every SM keeps two rows per team in flight
 // and no CTA is launched per row.  Per token, the team's absmax goes through
 // a named barrier of its own T threads (teams leave the loop independently),
 // with the shared partials double-buffered by row parity; per group (gs > 0)
 // a group is gs / 8 consecutive lanes of one warp, reduced with shuffles.
-template <int V, bool PG>
-__global__ void __launch_bounds__(256, V <= 2 ? 4 : 3) row_quant_half_rows(const uint4 *__restrict__ x, long R,
-                                                             int K, int gs, int T,
-                                                             __half *__restrict__ out,
-                                                             float *__restrict__ scale) {
-  asm volatile("griddepcontrol.launch_dependents;");
+template <int V, bool PG, int MODE>
+__global__ void __launch_bounds__(256, V <= 2 ? 4 : 3) row_quant_rows(const uint4 *__restrict__ x, long R,
+                                                        int K, int gs, int T,
+                                                        void *__restrict__ out,
+                                                        float *__restrict__ scale) {
+  static_assert(MODE == kOutHalf || MODE == kOutInt8, "activation modes");
+  // fp16 codes feed the GEMM: let it launch now (it waits for this grid
+  // before reading any input); the INT8 mode never starts dependents early
+  if (MODE == kOutHalf) asm volatile("griddepcontrol.launch_dependents;");
   __shared__ float red[2][8];
   const int nvec = K >> 3;
   const int G = gs == 0 ? 1 : K / gs;
@@ -201,16 +209,19 @@ __global__ void __launch_bounds__(256, V <= 2 ? 4 : 3) row_quant_half_rows(const
         }
         float q[8];
         quant_vec8(cur[i], sc, rc, q);
-        reinterpret_cast<uint4 *>(out + r * K)[vi] = pack_h8(q);
+        if (MODE == kOutHalf)
+          reinterpret_cast<uint4 *>(static_cast<__half *>(out) + r * K)[vi] = pack_h8(q);
+        else
+          reinterpret_cast<uint2 *>(static_cast<int8_t *>(out) + r * K)[vi] = pack_i8x8(q);
       }
       cur[i] = nxt[i];
     }
   }
 }
 
-template <int V, bool PG>
-int launch_rows_half(const __half *x, long R, int K, int gs, int T, __half *out, float *scale,
-                     cudaStream_t s) {
+template <int V, bool PG, int MODE>
+int launch_rows(const __half *x, long R, int K, int gs, int T, void *out, float *scale,
+                cudaStream_t s) {
   static int blocks[64] = {};
   static std::mutex mu;
   int dev = 0;
@@ -221,7 +232,7 @@ int launch_rows_half(const __half *x, long R, int K, int gs, int T, __half *out,
     if (blocks[dev] == 0) {
       int nsm = 0, occ = 0;
       if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, row_quant_half_rows<V, PG>, 256, 0) !=
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, row_quant_rows<V, PG, MODE>, 256, 0) !=
               cudaSuccess || occ < 1)
         return W8A8_ERR_CUDA;
       blocks[dev] = nsm * occ;
@@ -231,7 +242,7 @@ int launch_rows_half(const __half *x, long R, int K, int gs, int T, __half *out,
   const int teams = 256 / T;
   const long need = (R + teams - 1) / teams;
   const long grid = need < per_sm ? need : per_sm;
-  row_quant_half_rows<V, PG><<<static_cast<unsigned>(grid), 256, 0, s>>>(
+  row_quant_rows<V, PG, MODE><<<static_cast<unsigned>(grid), 256, 0, s>>>(
       reinterpret_cast<const uint4 *>(x), R, K, gs, T, out, scale);
   return launch_status();
 }
@@ -256,21 +267,21 @@ int launch_mode(const __half *x, int R, int K, int group_size, int qmax, void *o
   int T = 32;
   while (T < 256 && (nvec + T - 1) / T > 4) T <<= 1;
   const int V = (nvec + T - 1) / T;
-  if (MODE == kOutHalf && V <= 4) {
-    __half *qh = static_cast<__half *>(out);
+  if ((MODE == kOutHalf || MODE == kOutInt8) && qmax == 127 && V <= 4) {
+    constexpr int AM = MODE == kOutInt4 ? kOutInt8 : MODE;  // (INT4 never gets here)
     if (group_size != 0) {
       switch (V) {
-        case 1: return launch_rows_half<1, true>(x, R, K, group_size, T, qh, scale, s);
-        case 2: return launch_rows_half<2, true>(x, R, K, group_size, T, qh, scale, s);
-        case 3: return launch_rows_half<3, true>(x, R, K, group_size, T, qh, scale, s);
-        default: return launch_rows_half<4, true>(x, R, K, group_size, T, qh, scale, s);
+        case 1: return launch_rows<1, true, AM>(x, R, K, group_size, T, out, scale, s);
+        case 2: return launch_rows<2, true, AM>(x, R, K, group_size, T, out, scale, s);
+        case 3: return launch_rows<3, true, AM>(x, R, K, group_size, T, out, scale, s);
+        default: return launch_rows<4, true, AM>(x, R, K, group_size, T, out, scale, s);
       }
     }
     switch (V) {
-      case 1: return launch_rows_half<1, false>(x, R, K, 0, T, qh, scale, s);
-      case 2: return launch_rows_half<2, false>(x, R, K, 0, T, qh, scale, s);
-      case 3: return launch_rows_half<3, false>(x, R, K, 0, T, qh, scale, s);
-      default: return launch_rows_half<4, false>(x, R, K, 0, T, qh, scale, s);
+      case 1: return launch_rows<1, false, AM>(x, R, K, 0, T, out, scale, s);
+      case 2: return launch_rows<2, false, AM>(x, R, K, 0, T, out, scale, s);
+      case 3: return launch_rows<3, false, AM>(x, R, K, 0, T, out, scale, s);
+      default: return launch_rows<4, false, AM>(x, R, K, 0, T, out, scale, s);
     }
   }
   switch (V) {
