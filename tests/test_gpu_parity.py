@@ -479,7 +479,10 @@ def test_weight_only_exact_cases():
 @pytest.mark.parametrize("M,N,K,gs,wbits", [
     (1, 512, 512, 0, 8), (128, 512, 512, 0, 8), (5, 300, 2560, 128, 8), (1, 300, 2560, 64, 8),
     (300, 257, 4096, 0, 4), (1, 257, 4096, 0, 4), (1, 40, 32768, 64, 8), (1, 1000, 16, 0, 8),
-    (1, 333, 96, 0, 4)])
+    (1, 333, 96, 0, 4),
+    # decode with part of each warp's weight segment staged in shared memory
+    # and the rest streamed through registers
+    (1, 4096, 14336, 128, 8), (1, 28672, 4096, 0, 4), (1, 3000, 8192, 0, 8)])
 def test_linear_matches_oracle(M, N, K, gs, wbits):
     x = act(M, K, seed=3, n_outliers=4, outlier_scale=40.0)
     W = synth.weights(N, K, seed=4)

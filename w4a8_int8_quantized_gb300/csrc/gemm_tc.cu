@@ -101,7 +101,10 @@ struct Plan {
   static constexpr int STAGE_BYTES = W16_BYTES + X16_BYTES;
   // S: operand stages.  With KS = 1 a fourth measured no faster, and three
   // leave more of the SM's L1 to the per-group epilogue's scale loads.
-  static constexpr int S8 = KS == 1 ? 3 : 2, S = KS == 1 ? 3 : 2;
+  // S8: weight staging stages.  128-token tiles of two K blocks have room
+  // for a third (M = 128: 19.3 -> 17.9 us; a fourth gained nothing more,
+  // and a third operand stage in its place gained nothing).
+  static constexpr int S8 = KS == 1 ? 3 : (BT == 128 ? 3 : 2), S = KS == 1 ? 3 : 2;
 #ifndef W8A8_TC_RELEASE
   static constexpr int REL = 1;                    // stages released per commit
 #else
@@ -160,15 +163,29 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
 }
 
+// HINT: the waiting thread re-checks at least every 100 ns instead of
+// after the system-dependent suspend time (measured on GB300: the per
+// channel kernels ~2 % faster, the per-group ones ~4 % slower, so only the
+// former pass it).
+template <bool HINT = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (HINT)
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(100)
+        : "memory");
+  else
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
@@ -250,15 +267,16 @@ __device__ __forceinline__ void stg_b32(void *ptr, int v) {
 
 // Bounded wait.  Returns false if the CTA is aborting or the wait gave up
 // (then it records `code` and raises the abort flag).
+template <bool HINT = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity,
                                          volatile int *abort_flag, unsigned int code,
                                          unsigned int *err, long long limit) {
 #pragma unroll 1
   for (int i = 0; i < 32; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<HINT>(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<HINT>(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       if (err != nullptr) atomicCAS(err, 0u, code);
@@ -508,10 +526,10 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
         }
         if (n < p.N) sw_g = __ldg(p.sw + n * p.G + c);
       }
-      bool w = wait_bar(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err,
+      bool w = wait_bar<!PERGROUP>(accfull(r), (cc >> 1) & 1u, abort_flag, kDevErrAccumBarrier, p.err,
                         p.wait_limit);
       if (PERGROUP && want_y && STAGE_SA)
-        w = w && wait_bar(saready(gb), gph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
+        w = w && wait_bar<!PERGROUP>(saready(gb), gph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
@@ -587,7 +605,7 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, uint32_t tmem, 
       continue;
     }
     if (!PERGROUP && STAGE_SA) {
-      bool w = wait_bar(saready(sb), sph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
+      bool w = wait_bar<!PERGROUP>(saready(sb), sph, abort_flag, kDevErrAccumBarrier, p.err, p.wait_limit);
       if (!__all_sync(0xffffffffu, w)) break;
     }
     if (n >= p.N) continue;
@@ -726,7 +744,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
           const int nb = tile % p.nblocks, tb = tile / p.nblocks;
           for (int kb = 0; kb < nkb; ++kb) {
-            if (!wait_bar(empty8(s8), ph8 ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit)) {
+            if (!wait_bar<!PERGROUP>(empty8(s8), ph8 ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit)) {
               ok = false;
               break;
             }
@@ -761,7 +779,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kb = 0; kb < nkb; ++kb) {
             // a release group is refilled once the MMAs of its last use are done
             if ((s % REL) == 0 &&
-                !wait_bar(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit)) {
+                !wait_bar<!PERGROUP>(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit)) {
               ok = false;
               break;
             }
@@ -794,7 +812,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool first = (kb % chunk_kb) == 0;
             const uint32_t r = cc & 1u;
             if (first) {
-              if (!wait_bar(accempty(r), ((cc >> 1) & 1u) ^ 1u, abort_flag, kDevErrTmemEmpty,
+              if (!wait_bar<!PERGROUP>(accempty(r), ((cc >> 1) & 1u) ^ 1u, abort_flag, kDevErrTmemEmpty,
                             p.err, p.wait_limit)) {
                 ok = false;
                 break;
@@ -804,7 +822,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t d = tmem + r * BT;
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
-              if (!wait_bar(full(s, j), ph, abort_flag, kDevErrFullBarrier, p.err, p.wait_limit)) {
+              if (!wait_bar<!PERGROUP>(full(s, j), ph, abort_flag, kDevErrFullBarrier, p.err, p.wait_limit)) {
                 ok = false;
                 break;
               }
@@ -842,9 +860,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.ntiles && ok; tile += gridDim.x) {
         for (int kb = 0; kb < nkb; ++kb) {
-          bool w = wait_bar(full8(s8), ph8, abort_flag, kDevErrFullBarrier, p.err, p.wait_limit);
+          bool w = wait_bar<!PERGROUP>(full8(s8), ph8, abort_flag, kDevErrFullBarrier, p.err, p.wait_limit);
           if ((s % REL) == 0)
-            w = w && wait_bar(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit);
+            w = w && wait_bar<!PERGROUP>(empty(s / REL), ph ^ 1u, abort_flag, kDevErrEmptyBarrier, p.err, p.wait_limit);
           if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;

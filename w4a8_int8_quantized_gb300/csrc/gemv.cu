@@ -31,9 +31,12 @@
 //    are predicated in place and the row walk is selects.
 //  * When a row is a whole number of 32-chunk steps (K a multiple of 512 for
 //    INT8 weights, 1024 for INT4 -- every workload here), each step lies in
-//    one row: its exact int32 dot products (dp4a) with the activation codes
-//    are reduced over the warp (redux.sync) and lane 0 adds them to the row's
-//    accumulator in shared memory.  Per group, the 4 or 8 lanes of each
+//    one row: each lane adds its exact int32 dot products (dp4a) with the
+//    activation codes over the steps of a row, and when the row (or the
+//    warp's segment) ends the warp reduces them (redux.sync) and lane 0 adds
+//    the sum to the row's accumulator in shared memory (with 4 or 8
+//    activation rows, every step is reduced: the per-row partials would
+//    take the registers the loads need).  Per group, the 4 or 8 lanes of each
 //    K-group are reduced with xor shuffles and the group's first lane stores
 //    the sum.  Other row lengths take a general walk (a step may meet two or
 //    more rows).  int32 sums are exact, so the order of the additions is
@@ -103,6 +106,19 @@ __device__ __forceinline__ void red_shared_if(uint32_t addr, int v, bool pred) {
       "{\n.reg .pred p;\nsetp.ne.b32 p, %2, 0;\n"
       "@p red.shared.add.s32 [%0], %1;\n}\n" ::"r"(addr),
       "r"(v), "r"(static_cast<int>(pred))
+      : "memory");
+}
+
+// When `pred` (uniform over the warp): the warp's sum of v, added to the
+// shared int32 at addr by the lane with `lane0`.
+__device__ __forceinline__ void redux_red_if(uint32_t addr, int v, bool pred, bool lane0) {
+  asm volatile(
+      "{\n.reg .pred p, q;\n.reg .s32 t;\n"
+      "setp.ne.b32 p, %2, 0;\n"
+      "@p redux.sync.add.s32 t, %1, 0xffffffff;\n"
+      "setp.ne.and.b32 q, %3, 0, p;\n"
+      "@q red.shared.add.s32 [%0], t;\n}\n" ::"r"(addr),
+      "r"(v), "r"(static_cast<int>(pred)), "r"(static_cast<int>(lane0))
       : "memory");
 }
 
@@ -478,12 +494,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) mv_kernel(
     // shuffles) is stored by the run's first lane, and by no other step.
     int row = crow, col = ckc;
     const uint32_t acc_s = smem_u32(acc);
+    // per channel with one or two activation rows, each lane sums its dot
+    // products over the steps of a row and the warp reduces once per row
+    // (when the row ends, or the segment); with more rows (their partials
+    // would take the registers) the warp reduces every step
+    constexpr bool ROWSUM = MR <= 2;
+    int racc[MR];
+#pragma unroll
+    for (int m = 0; m < MR; ++m) racc[m] = 0;
     for (int j0 = 0; j0 < nsteps; j0 += U) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = j0 + u;
         const bool valid = j < nsteps;  // uniform over the warp
         const int kl = col + lane;      // in [0, cpr) whatever j is
+        const int c2 = col + 32;
+        const bool wrap = c2 == cpr;    // this step ends its row
         if (PERGROUP) {
           const int cpg = gs >> 4;
           int d = dot16(buf[u], xs4[kl]);
@@ -496,16 +522,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) mv_kernel(
             const int d = WBITS == 8 ? dot16(buf[u], xs4[m * kv + kl])
                                      : dot32_w4u(buf[u], xs4[m * kv + 2 * kl],
                                                  xs4[m * kv + 2 * kl + 1]);
-            const int t = __reduce_add_sync(0xffffffffu, d);
-            red_shared_if(acc_s + 4u * static_cast<uint32_t>(row * MR + m), t, valid && lane == 0);
+            if (ROWSUM) {
+              racc[m] += valid ? d : 0;
+              redux_red_if(acc_s + 4u * static_cast<uint32_t>(row * MR + m), racc[m],
+                           valid && wrap, lane == 0);
+              racc[m] = valid && wrap ? 0 : racc[m];
+            } else {
+              const int t = __reduce_add_sync(0xffffffffu, d);
+              red_shared_if(acc_s + 4u * static_cast<uint32_t>(row * MR + m), t,
+                            valid && lane == 0);
+            }
           }
         }
         ldg_stream_if(wg + 32 * (j + U), buf[u], j + U < nsteps);
-        col += 32;
-        const bool wrap = col == cpr;
-        col = wrap ? 0 : col;
-        row += wrap ? 1 : 0;
+        col = valid ? (wrap ? 0 : c2) : col;
+        row += valid && wrap ? 1 : 0;
       }
+    }
+    // the row the segment ends in, when it ends inside one
+    if (!PERGROUP && ROWSUM) {
+#pragma unroll
+      for (int m = 0; m < MR; ++m)
+        redux_red_if(acc_s + 4u * static_cast<uint32_t>(row * MR + m), racc[m], row < rows,
+                     lane == 0);
     }
   } else {
     for (int j0 = 0; j0 < nsteps; j0 += U) {
