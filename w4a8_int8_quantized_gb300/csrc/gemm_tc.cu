@@ -105,11 +105,7 @@ struct Plan {
   // for a third (M = 128: 19.3 -> 17.9 us; a fourth gained nothing more,
   // and a third operand stage in its place gained nothing).
   static constexpr int S8 = KS == 1 ? 3 : (BT == 128 ? 3 : 2), S = KS == 1 ? 3 : 2;
-#ifndef W8A8_TC_RELEASE
   static constexpr int REL = 1;                    // stages released per commit
-#else
-  static constexpr int REL = W8A8_TC_RELEASE;
-#endif
   // warp roles: 0 producers (lane 0 staging, lane 1 fp16 activations), 1
   // MMA, 2-7 converters, 8-15 epilogue
   static constexpr int CONV_WARPS = 6;
