@@ -17,8 +17,11 @@ value    = sum over the sweep of 2*M*N*K integer ops / device time of the step
            the two kernels.
 e2e      = the same metric through the C ABI's ``linear`` call with pinned
            host buffers: host->device copy of x, the layer, device->host copy
-           of y, all inside the timed events; from M = 2048 on, in chunks of
-           1024 rows whose copies and layer calls overlap on three streams.
+           of y, all inside the timed events; from M = 1024 on, in chunks of
+           512 rows whose copies and layer calls overlap on three streams.
+           The copies and linear() calls of each M are captured once into a
+           CUDA graph and replayed every step (eager_value: the same calls
+           enqueued by the host every step).
 roofline = the dominant kernel (the GEMM at M=8192): 2*M*N*K / its average
            CUDA-event duration in the breakdown pass, against the measured
            dense fp16/bf16 tensor peak; traffic = DRAM bytes per launch from
@@ -616,13 +619,19 @@ def run_ours(args):
                          K_IN, 0, 8, P(b["ws"].data_ptr()), b["ws"].numel(), P(y.data_ptr()),
                          sptr), "linear")
 
-    def e2e_call(m, e0):
+    def e2e_call(m, e0, origin):
+        """One M end to end: copy-in, linear(), copy-out.  `origin` is the
+        stream the call starts and ends on (e0 is recorded there)."""
         b = bufs[m]
         C = e2e_chunks(m)
         if C == 1:
-            b["x"].copy_(b["xh"], non_blocking=True)
-            call_linear(m, b["x"], b["y"])
-            b["yh"].copy_(b["y"], non_blocking=True)
+            with torch.cuda.stream(origin):
+                b["x"].copy_(b["xh"], non_blocking=True)
+            check(lib.linear(P(b["x"].data_ptr()), P(wq.data_ptr()), P(sw.data_ptr()), m, N_OUT,
+                             K_IN, 0, 8, P(b["ws"].data_ptr()), b["ws"].numel(),
+                             P(b["y"].data_ptr()), P(origin.cuda_stream)), "linear")
+            with torch.cuda.stream(origin):
+                b["yh"].copy_(b["y"], non_blocking=True)
             return
         for st in (s_h2d, s_comp, s_d2h):
             st.wait_event(e0)
@@ -643,15 +652,21 @@ def run_ours(args):
         for st in (s_h2d, s_comp, s_d2h):
             ev = torch.cuda.Event()
             ev.record(st)
-            stream.wait_event(ev)
+            origin.wait_event(ev)
 
-    def e2e_step(record):
+    def e2e_step(record, graphs=None):
+        # eager: the host enqueues every copy and linear() call of every
+        # chunk; graphs: each M's calls were captured once into a CUDA graph
+        # (the same linear() calls and host copies), replayed here
         evs = []
         for m in MS:
             flush_l2()
             e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
             e0.record(stream)
-            e2e_call(m, e0)
+            if graphs is None:
+                e2e_call(m, e0, stream)
+            else:
+                graphs[m].replay()
             e1.record(stream)
             evs.append((m, e0, e1))
         if record is not None:
@@ -699,18 +714,38 @@ def run_ours(args):
             per_m[m]["quant_ms"] += e0.elapsed_time(e1) / n_split
             per_m[m]["gemm_ms"] += e1.elapsed_time(e2) / n_split
 
-    # e2e through linear() with host buffers
-    for _ in range(2):
-        e2e_step(None)
-    rec2 = []
-    torch.cuda.synchronize()
-    torch.cuda._sleep(int(2e6))
-    for _ in range(args.steps):
-        e2e_step(rec2)
-    torch.cuda.synchronize()
-    e2e_ms = sum(e0.elapsed_time(e1) for evs in rec2 for _, e0, e1 in evs) / args.steps
-    e2e_ms = max_over_ranks(e2e_ms, ws, device)
-    e2e_value = ws * step_ops() / (e2e_ms * 1e-3) / 1e12
+    # e2e through linear() with host buffers: eager, then as CUDA graphs
+    def e2e_measure(graphs):
+        for _ in range(2):
+            e2e_step(None, graphs)
+        rec2 = []
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e6))
+        for _ in range(args.steps):
+            e2e_step(rec2, graphs)
+        torch.cuda.synchronize()
+        ms = sum(e0.elapsed_time(e1) for evs in rec2 for _, e0, e1 in evs) / args.steps
+        ms = max_over_ranks(ms, ws, device)
+        return ws * step_ops() / (ms * 1e-3) / 1e12
+
+    e2e_eager = e2e_measure(None)
+    e2e_value, e2e_graph_error = e2e_eager, None
+    if not args.e2e_eager_only:
+        try:
+            graphs = {}
+            for m in MS:
+                g = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream()
+                with torch.cuda.graph(g, stream=cap):
+                    fork = torch.cuda.Event()
+                    fork.record(cap)
+                    e2e_call(m, fork, cap)
+                graphs[m] = g
+            torch.cuda.synchronize()
+            e2e_value = e2e_measure(graphs)
+        except RuntimeError as ex:  # capture refused: report the eager number and why
+            e2e_graph_error = str(ex).splitlines()[0][:200]
+            torch.cuda.synchronize()
     # the outputs the chunked three-stream path copied back must equal one
     # linear() call over all rows on one stream (bit for bit: the rows of a
     # chunk are computed exactly as in the whole call)
@@ -798,10 +833,16 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 3), "unit": UNIT,
                     "h2d_bytes_per_step": sum(m * K_IN * 2 for m in MS),
                     "d2h_bytes_per_step": sum(m * N_OUT * 2 for m in MS),
-                    "method": f"C ABI linear() per M from pinned host buffers, L2 flushed "
-                              f"before each M; M >= {2 * chunk_rows} in chunks of "
-                              f"{chunk_rows} rows with copy-in, layer and copy-out "
-                              f"overlapped on three streams",
+                    "method": (f"C ABI linear() per M from pinned host buffers, L2 flushed "
+                               f"before each M; M >= {2 * chunk_rows} in chunks of "
+                               f"{chunk_rows} rows with copy-in, layer and copy-out "
+                               f"overlapped on three streams; "
+                               + ("the calls and copies of each M captured once into a "
+                                  "CUDA graph and replayed every step"
+                                  if e2e_graph_error is None and not args.e2e_eager_only
+                                  else "enqueued by the host every step")),
+                    "eager_value": round(e2e_eager, 3),
+                    "graph_capture_error": e2e_graph_error,
                     "outputs_equal_single_stream_linear": e2e_mismatch == 0,
                     "mismatched_outputs": e2e_mismatch},
             "gpu_launches": args.steps * (2 * len(MS) - 1),  # M=1 is one fused launch
@@ -885,6 +926,8 @@ def main():
                     help="run one kernel of the path on one shape (for profilers)")
     ap.add_argument("--e2e-chunk-rows", type=int, default=E2E_CHUNK_ROWS,
                     help="rows per pipelined chunk of the end-to-end measurement")
+    ap.add_argument("--e2e-eager-only", action="store_true",
+                    help="time the end-to-end path as enqueued by the host only (no CUDA graphs)")
     ap.add_argument("--m", type=int, default=8192)
     ap.add_argument("--n", type=int, default=N_OUT)
     ap.add_argument("--k", type=int, default=K_IN)
